@@ -1,0 +1,252 @@
+"""Pins for the fp64 selection/decode oracle (CPU only).
+
+Each test ties the oracle to something other than itself: numbers the
+InfiniteHiP summary prints, a library routine (torch SDPA in float64), a
+brute-force characterisation on tiny inputs, or an invariant the pages state.
+"""
+import itertools
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import hip
+from oracle.numerics import to_f64
+from synth import decode_case, decode_tiny
+
+
+def _f64_keys(rng, T, H_kv, D):
+    return rng.standard_normal((T, H_kv, D)).astype(np.float32)
+
+
+# ------------------------------------------------------------ page counts
+
+def test_candidate_range_page_counts(golden):
+    g = golden["sink_stream_1m"]
+    I = hip.candidate_range(g["T"], g["n_sink"], g["n_stream"])
+    assert len(I) == g["pruned_tokens"]
+    A = hip.attended_set(g["T"], g["n_sink"], g["n_stream"], np.zeros(0, np.int64))
+    assert len(A) == g["always_kept_tokens"]
+    assert I[0] == g["n_sink"] and I[-1] == g["T"] - g["n_stream"] - 1
+
+
+def test_stage_chunk_counts_at_1m(golden):
+    g = golden["stage_chunk_counts_1m"]
+    I = hip.candidate_range(g["T"], g["n_sink"], g["n_stream"])
+    n_chunks = []
+    for L, k in zip(g["chunk"], g["keep"]):
+        chunks = hip.chunk_partition(I, L)
+        n_chunks.append(len(chunks))
+        Kc = k // L
+        # keep the first K chunks: the count of surviving tokens is what matters here
+        I = hip.assemble(chunks, np.arange(min(Kc, len(chunks))))
+        assert len(I) <= k
+    for got, want in zip(n_chunks, g["approx_chunks_per_stage"]):
+        assert abs(got - want) <= g["rel_tol"] * want
+    assert abs(sum(n_chunks) - g["approx_total"]) <= g["rel_tol"] * g["approx_total"]
+
+
+def test_window_sizes(golden):
+    g = golden["window_size_3k_5k"]
+    for keep, total in zip(g["final_keep"], g["total_window"]):
+        T = 1 << 20
+        I = np.arange(g["n_sink"], g["n_sink"] + keep)
+        assert len(hip.attended_set(T, g["n_sink"], g["n_stream"], I)) == total
+
+
+@pytest.mark.parametrize("case", [0, 1])
+def test_selectrep_evaluation_count(golden, case):
+    c = golden["selectrep_evaluations"]["cases"][case]
+    L = c["l_c"]
+    rng = np.random.default_rng(10 + case)
+    K = _f64_keys(rng, L, 1, 16)
+    q = rng.standard_normal((3, 16))
+    r, rho, evals = hip.select_rep(q, K[:, 0, :], "f32", np.arange(L))
+    assert evals == c["evaluations"] == 2 * math.ceil(math.log2(L))
+
+
+# ------------------------------------------------------------ tournament characterisation
+
+def _leaf_path_ok(scores, r):
+    """Independent characterisation of the tournament winner by enumeration.
+
+    For leaf r, walk the halving tree: at every split of the range holding r,
+    r's half must win (right half wins only on a strictly larger first score).
+    """
+    a, b = 0, len(scores) - 1
+    while a < b:
+        mid = (a + b + 1) // 2
+        right_wins = scores[mid] > scores[a]
+        if r >= mid and not right_wins:
+            return False
+        if r < mid and right_wins:
+            return False
+        a, b = (mid, b) if r >= mid else (a, mid - 1)
+    return True
+
+
+@pytest.mark.parametrize("L", [1, 2, 3, 4, 5, 7, 8, 11, 16])
+def test_selectrep_matches_enumeration(L):
+    rng = np.random.default_rng(L)
+    D = 8
+    for trial in range(40):
+        # integer-valued keys so that ties really occur
+        K = rng.integers(-2, 3, size=(L, D)).astype(np.float32)
+        q = rng.integers(-2, 3, size=(2, D)).astype(np.float64)
+        scores = np.max(q @ K.astype(np.float64).T, axis=0)
+        winners = [r for r in range(L) if _leaf_path_ok(scores, r)]
+        assert len(winners) == 1
+        pos = np.arange(100, 100 + L)
+        r, rho, _ = hip.select_rep(q, np.concatenate([np.zeros((100, D), np.float32), K]),
+                                   "f32", pos)
+        assert r == 100 + winners[0]
+        assert rho == scores[winners[0]]
+
+
+def test_selectrep_special_orders():
+    D, L = 4, 16
+    q = np.ones((1, D))
+    inc = np.repeat(np.arange(L, dtype=np.float32)[:, None], D, axis=1)
+    assert hip.select_rep(q, inc, "f32", np.arange(L))[0] == L - 1   # increasing -> last
+    assert hip.select_rep(q, inc[::-1].copy(), "f32", np.arange(L))[0] == 0  # decreasing -> first
+    flat = np.ones((L, D), np.float32)
+    assert hip.select_rep(q, flat, "f32", np.arange(L))[0] == 0     # all tied -> left wins
+
+
+@pytest.mark.parametrize("L", [1, 2])
+def test_selectrep_exact_for_tiny_chunks(L):
+    rng = np.random.default_rng(5)
+    for _ in range(50):
+        K = rng.standard_normal((L, 6)).astype(np.float32)
+        q = rng.standard_normal((4, 6))
+        s = np.max(q @ K.astype(np.float64).T, axis=0)
+        assert hip.select_rep(q, K, "f32", np.arange(L))[0] == int(np.argmax(s))
+
+
+def test_vectorised_tournament_equals_scalar():
+    c = decode_case("t", B=1, T=700, T_q=2, H_q=4, H_kv=2, D=16, dtype="bf16",
+                    chunk=(16,), keep=(64,), n_sink=4, n_stream=8, seed=7, plant="none")
+    q = to_f64(c.q[0], "bf16")
+    I = hip.candidate_range(700, 4, 8)
+    for L in (1, 3, 16, 37):
+        chunks = hip.chunk_partition(I, L)
+        reps, rho = hip.select_rep_all(q, c.k[0], "bf16", chunks, c.G)
+        for h in range(4):
+            for j in range(0, len(chunks), 5):
+                r, s, _ = hip.select_rep(q[:, h, :], c.k[0][:, h // c.G, :], "bf16", chunks[j])
+                assert reps[h, j] == r and rho[h, j] == s
+
+
+# ------------------------------------------------------------ top-K characterisation
+
+def test_topk_pairwise_characterisation():
+    rng = np.random.default_rng(3)
+    for n in range(1, 9):
+        for K in range(1, n + 2):
+            for _ in range(10):
+                s = rng.integers(0, 4, size=n).astype(np.float64)
+                kept = hip.topk_chunks(s, K)
+                assert list(kept) == sorted(kept)
+                assert len(kept) == min(n, K)
+                ks = set(kept.tolist())
+                for i in ks:
+                    for j in set(range(n)) - ks:
+                        assert s[i] > s[j] or (s[i] == s[j] and i < j)
+
+
+def test_topk_matches_exhaustive_subsets():
+    rng = np.random.default_rng(4)
+    n, K = 7, 3
+    for _ in range(30):
+        s = rng.integers(0, 3, size=n).astype(np.float64)
+        # best subset: largest sum of scores, then lexicographically smallest indices
+        best = min(itertools.combinations(range(n), K),
+                   key=lambda c: (-sum(s[list(c)]), sorted(c)))
+        assert list(hip.topk_chunks(s, K)) == sorted(best)
+
+
+# ------------------------------------------------------------ invariants + dense case
+
+def _run(c, b=0):
+    q = to_f64(c.q[b], c.dtype)
+    stages, I = hip.hip_select(q, c.k[b], c.dtype, int(c.kv_len[b]), c.chunk, c.keep,
+                               c.n_sink, c.n_stream, c.G)
+    return q, stages, I
+
+
+def test_stage_invariants_tiny_config():
+    c = decode_tiny()
+    q, stages, I = _run(c)
+    prev = hip.candidate_range(2048, c.n_sink, c.n_stream)
+    for st, k in zip(stages, c.keep):
+        assert len(st.I_out) <= k
+        assert np.all(np.diff(st.I_out) > 0)
+        assert np.all(np.isin(st.I_out, prev))
+        prev = st.I_out
+    A = hip.attended_set(2048, c.n_sink, c.n_stream, I)
+    assert len(A) == 16 + 128 + 64
+    assert np.all(np.isin(np.arange(16), A)) and np.all(np.isin(np.arange(2048 - 64, 2048), A))
+
+
+def test_dense_special_case_matches_sdpa():
+    """keep >= all chunks at every stage -> attention over every key == dense SDPA."""
+    c = decode_case("dense", B=1, T=300, T_q=3, H_q=4, H_kv=2, D=32, dtype="bf16",
+                    chunk=(16, 4), keep=(4096, 4096), n_sink=5, n_stream=7, seed=11,
+                    plant="none")
+    q, stages, I = _run(c)
+    assert np.array_equal(I, hip.candidate_range(300, 5, 7))
+    A = hip.attended_set(300, 5, 7, I)
+    assert np.array_equal(A, np.arange(300))
+    O, lse = hip.decode_attention(q, c.k[0], c.v[0], "bf16", A, c.scale, c.G)
+    Qt = torch.from_numpy(q).permute(1, 0, 2)                       # [H, T_q, D]
+    Kt = torch.from_numpy(to_f64(c.k[0], "bf16")).permute(1, 0, 2)  # [H_kv, T, D]
+    Vt = torch.from_numpy(to_f64(c.v[0], "bf16")).permute(1, 0, 2)
+    Kt = Kt.repeat_interleave(c.G, 0)
+    Vt = Vt.repeat_interleave(c.G, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(Qt, Kt, Vt)
+    np.testing.assert_allclose(O, ref.permute(1, 0, 2).numpy(), rtol=0, atol=1e-12)
+    ref_lse = torch.logsumexp(c.scale * Qt @ Kt.transpose(1, 2), dim=-1)
+    np.testing.assert_allclose(lse, ref_lse.T.numpy(), rtol=0, atol=1e-12)
+
+
+def test_exact_exclusion_matches_eq1_constant():
+    """Exact exclusion == softmax(QK^T/sqrt(d) - c(1-M)) with c = 1e5 (MInference Eq. 1)."""
+    rng = np.random.default_rng(12)
+    T, D = 200, 32
+    K = rng.standard_normal((T, 1, D)).astype(np.float32)
+    V = rng.standard_normal((T, 1, D)).astype(np.float32)
+    q = rng.standard_normal((2, 1, D))
+    A = np.sort(rng.choice(T, 40, replace=False))
+    O, _ = hip.decode_attention(q, K, V, "f32", A, 1 / np.sqrt(D), 1)
+    M = np.zeros(T)
+    M[A] = 1
+    z = torch.from_numpy(q[:, 0] @ K[:, 0].astype(np.float64).T / np.sqrt(D) - 1e5 * (1 - M))
+    ref = torch.softmax(z, -1).numpy() @ V[:, 0].astype(np.float64)
+    np.testing.assert_allclose(O[:, 0], ref, rtol=0, atol=1e-12)
+
+
+def test_metamorphic_scale_and_shift():
+    c = decode_case("meta", B=1, T=900, T_q=1, H_q=4, H_kv=1, D=32, dtype="f32",
+                    chunk=(32, 8), keep=(256, 64), n_sink=8, n_stream=16, seed=13)
+    q, stages, I = _run(c)
+    stages2, I2 = hip.hip_select(2.5 * q, c.k[0], "f32", 900, c.chunk, c.keep, 8, 16, c.G)
+    assert np.array_equal(I, I2)
+    for a, b in zip(stages, stages2):
+        assert np.array_equal(a.reps, b.reps) and np.array_equal(a.kept, b.kept)
+    A = hip.attended_set(900, 8, 16, I)
+    O, _ = hip.decode_attention(q, c.k[0], c.v[0], "f32", A, c.scale, c.G)
+    V2 = (c.v[0].astype(np.float64) + 0.75)
+    O2, _ = hip.decode_attention(q, c.k[0], V2, "f64", A, c.scale, c.G)
+    np.testing.assert_allclose(O2, O + 0.75, rtol=0, atol=1e-12)
+
+
+def test_partial_chunk_and_short_context():
+    # context shorter than sink + window: nothing to prune, everything attended once
+    I = hip.candidate_range(50, 32, 64)
+    assert len(I) == 0
+    A = hip.attended_set(50, 32, 64, I)
+    assert np.array_equal(A, np.arange(50))
+    # ragged last chunk keeps its true length
+    chunks = hip.chunk_partition(np.arange(10, 31), 8)
+    assert [len(x) for x in chunks] == [8, 8, 5]
