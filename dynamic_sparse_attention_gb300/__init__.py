@@ -1,0 +1,22 @@
+"""GB300-native dynamic sparse attention: InfiniteHiP chunk-pruned decode and
+MInference vertical-slash prefill, as hand-written sm_103a kernels behind a C ABI.
+
+The Python surface mirrors the C entry points in ``include/dsa.h`` one to one;
+it only marshals torch CUDA tensors into pointers.  Importing this package
+does not load the library; the first call does, and raises if the library
+has not been built (``__graft_entry__.build()``).
+"""
+from .binding import (  # noqa: F401
+    DsaError,
+    HipConfig,
+    hip_max_chunks,
+    hip_select,
+    hip_select_workspace_bytes,
+    library_path,
+    load,
+    sparse_attn_decode,
+    sparse_attn_decode_workspace_bytes,
+    sparse_attn_prefill,
+    vs_index_build,
+    vs_index_build_workspace_bytes,
+)

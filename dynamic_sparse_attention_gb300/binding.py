@@ -1,0 +1,339 @@
+"""ctypes binding of libdsa.so: argument marshalling only.
+
+Every step of the hot path runs in the CUDA kernels behind the C ABI
+(``include/dsa.h``).  This module turns torch CUDA tensors into device
+pointers, allocates the scratch workspace the library asks for (unless the
+caller passes one) and forwards the current torch stream.  There is no CPU
+fallback: if the library is missing or a call fails, an exception is raised.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import torch
+
+from . import _build
+
+MAX_STAGES = 8
+BF16, F32 = 0, 1
+
+_c_int = ctypes.c_int
+_vp = ctypes.c_void_p
+
+
+class DecodeShape(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("T_max", _c_int), ("T_q", _c_int), ("H_q", _c_int),
+                ("H_kv", _c_int), ("D", _c_int), ("dtype", _c_int)]
+
+
+class HipCfg(ctypes.Structure):
+    _fields_ = [("n_stages", _c_int), ("chunk", _c_int * MAX_STAGES),
+                ("keep", _c_int * MAX_STAGES), ("n_sink", _c_int), ("n_stream", _c_int)]
+
+
+class HipDebug(ctypes.Structure):
+    _fields_ = [("stage_idx", _vp * MAX_STAGES), ("stage_cnt", _vp * MAX_STAGES),
+                ("chunk_score", _vp * MAX_STAGES), ("rep", _vp * MAX_STAGES),
+                ("rep_score", _vp * MAX_STAGES)]
+
+
+class PrefillShape(ctypes.Structure):
+    _fields_ = [("B", _c_int), ("S", _c_int), ("H_q", _c_int), ("H_kv", _c_int), ("D", _c_int)]
+
+
+class VsCfg(ctypes.Structure):
+    _fields_ = [("last_q", _c_int), ("n_vertical", _c_int), ("n_slash", _c_int), ("block", _c_int)]
+
+
+class VsDebug(ctypes.Structure):
+    _fields_ = [("vsum", _vp), ("ssum", _vp)]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed with status {status}: {msg}")
+        self.status = status
+
+
+_lib = None
+
+# name -> (restype, argtypes)
+_SIGNATURES = {
+    "dsa_version": (_c_int, []),
+    "dsa_last_error": (ctypes.c_char_p, []),
+    "dsa_strerror": (ctypes.c_char_p, [_c_int]),
+    "dsa_hip_max_chunks": (_c_int, [_vp, _vp, _c_int, ctypes.POINTER(_c_int)]),
+    "hip_select_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
+    "hip_select": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "sparse_attn_decode_workspace": (_c_int, [_vp, _c_int, _c_int, _c_int,
+                                              ctypes.POINTER(ctypes.c_size_t)]),
+    "sparse_attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                    ctypes.c_float, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "vs_index_build_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
+    "vs_index_build": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
+                                ctypes.c_size_t, _vp]),
+    "sparse_attn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                     _vp, ctypes.c_float, _vp, _vp, _vp]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_missing: bool = False):
+    """Load libdsa.so (building it first if asked and absent)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.LIB
+    if not os.path.exists(path):
+        if not build_if_missing:
+            raise ImportError(f"libdsa.so not built ({path}); run __graft_entry__.build()")
+        _build.build()
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name, None)
+        if fn is None:
+            continue  # reported by exported_symbols(); calling it raises AttributeError
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def exported_symbols() -> dict:
+    """Which C entry points of the binding the loaded library exports."""
+    lib = load()
+    return {name: hasattr(lib, name) for name in _SIGNATURES}
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        msg = _lib.dsa_last_error().decode(errors="replace")
+        raise DsaError(fn, status, msg)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return BF16
+    if t.dtype == torch.float32:
+        return F32
+    raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("tensors must be contiguous CUDA tensors")
+
+
+def _workspace(nbytes: int, device, ws):
+    if ws is not None:
+        if ws.numel() * ws.element_size() < nbytes:
+            raise ValueError(f"workspace too small: {nbytes} bytes needed")
+        return ws
+    return torch.empty(max(nbytes, 1), dtype=torch.uint8, device=device)
+
+
+# ----------------------------------------------------------------------------- decode
+
+@dataclass
+class HipConfig:
+    chunk: tuple
+    keep: tuple
+    n_sink: int
+    n_stream: int
+
+    def c(self) -> HipCfg:
+        cfg = HipCfg()
+        cfg.n_stages = len(self.chunk)
+        for i, (c, k) in enumerate(zip(self.chunk, self.keep)):
+            cfg.chunk[i] = int(c)
+            cfg.keep[i] = int(k)
+        cfg.n_sink = int(self.n_sink)
+        cfg.n_stream = int(self.n_stream)
+        return cfg
+
+
+def decode_shape(q: torch.Tensor, k: torch.Tensor) -> DecodeShape:
+    B, T_q, H_q, D = q.shape
+    T_max, H_kv = k.shape[1], k.shape[2]
+    return DecodeShape(B, T_max, T_q, H_q, H_kv, D, _dtype_code(q))
+
+
+def hip_select_workspace_bytes(q, k, cfg: HipConfig) -> int:
+    lib = load()
+    n = ctypes.c_size_t()
+    shape, c = decode_shape(q, k), cfg.c()
+    _check("hip_select_workspace", lib.hip_select_workspace(ctypes.byref(shape), ctypes.byref(c),
+                                                             ctypes.byref(n)))
+    return n.value
+
+
+def hip_max_chunks(q, k, cfg: HipConfig, stage: int) -> int:
+    lib = load()
+    n = _c_int()
+    shape, c = decode_shape(q, k), cfg.c()
+    _check("dsa_hip_max_chunks", lib.dsa_hip_max_chunks(ctypes.byref(shape), ctypes.byref(c),
+                                                         stage, ctypes.byref(n)))
+    return n.value
+
+
+def hip_select(q, k, kv_len, cfg: HipConfig, *, debug: bool = False, out=None, workspace=None,
+               stream=None):
+    """Run all pruning stages; returns (sel_idx [B, keep[-1]], sel_cnt [B][, debug dict])."""
+    lib = load()
+    _need_cuda(q, k, kv_len)
+    shape, c = decode_shape(q, k), cfg.c()
+    B = shape.B
+    dev = q.device
+    if out is None:
+        sel_idx = torch.empty(B, cfg.keep[-1], dtype=torch.int32, device=dev)
+        sel_cnt = torch.empty(B, dtype=torch.int32, device=dev)
+    else:
+        sel_idx, sel_cnt = out
+    dbg = None
+    dbg_t = None
+    if debug:
+        dbg = HipDebug()
+        dbg_t = {"stage_idx": [], "stage_cnt": [], "chunk_score": [], "rep": [], "rep_score": []}
+        for i in range(len(cfg.chunk)):
+            mc = hip_max_chunks(q, k, cfg, i)
+            t = {
+                "stage_idx": torch.full((B, cfg.keep[i]), -7, dtype=torch.int32, device=dev),
+                "stage_cnt": torch.full((B,), -7, dtype=torch.int32, device=dev),
+                "chunk_score": torch.full((B, max(mc, 1)), float("nan"), device=dev),
+                "rep": torch.full((B, shape.H_q, max(mc, 1)), -7, dtype=torch.int32, device=dev),
+                "rep_score": torch.full((B, shape.H_q, max(mc, 1)), float("nan"), device=dev),
+            }
+            for key, v in t.items():
+                dbg_t[key].append(v)
+                getattr(dbg, key)[i] = v.data_ptr()
+    nbytes = hip_select_workspace_bytes(q, k, cfg)
+    ws = _workspace(nbytes, dev, workspace)
+    st = lib.hip_select(_ptr(q), _ptr(k), _ptr(kv_len), ctypes.byref(shape), ctypes.byref(c),
+                        _ptr(sel_idx), _ptr(sel_cnt), ctypes.byref(dbg) if dbg else None,
+                        _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check("hip_select", st)
+    if debug:
+        return sel_idx, sel_cnt, dbg_t
+    return sel_idx, sel_cnt
+
+
+def sparse_attn_decode_workspace_bytes(q, k, max_sel: int, n_sink: int, n_stream: int) -> int:
+    lib = load()
+    n = ctypes.c_size_t()
+    shape = decode_shape(q, k)
+    _check("sparse_attn_decode_workspace",
+           lib.sparse_attn_decode_workspace(ctypes.byref(shape), max_sel, n_sink, n_stream,
+                                            ctypes.byref(n)))
+    return n.value
+
+
+def sparse_attn_decode(q, k, v, kv_len, sel_idx, sel_cnt, *, n_sink: int, n_stream: int,
+                       scale: float | None = None, out=None, lse=None, want_lse: bool = True,
+                       workspace=None, stream=None):
+    """Attention over sink + selected + window keys; returns (out, lse or None)."""
+    lib = load()
+    _need_cuda(q, k, v, kv_len, sel_idx, sel_cnt)
+    shape = decode_shape(q, k)
+    max_sel = sel_idx.shape[1] if sel_idx is not None else 0
+    if scale is None:
+        scale = shape.D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(shape.B, shape.T_q, shape.H_q, dtype=torch.float32, device=q.device)
+    nbytes = sparse_attn_decode_workspace_bytes(q, k, max_sel, n_sink, n_stream)
+    ws = _workspace(nbytes, q.device, workspace)
+    st = lib.sparse_attn_decode(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_len), _ptr(sel_idx),
+                                _ptr(sel_cnt), max_sel, n_sink, n_stream, ctypes.c_float(scale),
+                                ctypes.byref(shape), _ptr(out), _ptr(lse), _ptr(ws),
+                                ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check("sparse_attn_decode", st)
+    return out, lse
+
+
+# ----------------------------------------------------------------------------- prefill
+
+def prefill_shape(q: torch.Tensor, k: torch.Tensor) -> PrefillShape:
+    B, S, H_q, D = q.shape
+    return PrefillShape(B, S, H_q, k.shape[2], D)
+
+
+def vs_index_build_workspace_bytes(q, k, last_q, n_vertical, n_slash, block=64) -> int:
+    lib = load()
+    n = ctypes.c_size_t()
+    shape = prefill_shape(q, k)
+    cfg = VsCfg(last_q, n_vertical, n_slash, block)
+    _check("vs_index_build_workspace",
+           lib.vs_index_build_workspace(ctypes.byref(shape), ctypes.byref(cfg), ctypes.byref(n)))
+    return n.value
+
+
+def vs_index_build(q, k, *, last_q: int = 64, n_vertical: int, n_slash: int, block: int = 64,
+                   debug: bool = False, out: dict | None = None, workspace=None, stream=None):
+    """Vertical-slash index and its tile/column lists; returns a dict of tensors."""
+    lib = load()
+    _need_cuda(q, k)
+    shape = prefill_shape(q, k)
+    B, S, H_q = shape.B, shape.S, shape.H_q
+    nq = (S + block - 1) // block
+    dev = q.device
+    if out is None:
+        out = {
+            "vertical": torch.empty(B, H_q, n_vertical, dtype=torch.int32, device=dev),
+            "slash": torch.empty(B, H_q, n_slash, dtype=torch.int32, device=dev),
+            "blk_cnt": torch.empty(B, H_q, nq, dtype=torch.int32, device=dev),
+            "blk_idx": torch.empty(B, H_q, nq, nq, dtype=torch.int32, device=dev),
+            "col_cnt": torch.empty(B, H_q, nq, dtype=torch.int32, device=dev),
+            "col_idx": torch.empty(B, H_q, nq, max(n_vertical, 1), dtype=torch.int32, device=dev),
+        }
+    dbg = None
+    if debug:
+        out["vsum"] = torch.empty(B, H_q, S, dtype=torch.float32, device=dev)
+        out["ssum"] = torch.empty(B, H_q, S, dtype=torch.float32, device=dev)
+        dbg = VsDebug(out["vsum"].data_ptr(), out["ssum"].data_ptr())
+    cfg = VsCfg(last_q, n_vertical, n_slash, block)
+    ws = _workspace(vs_index_build_workspace_bytes(q, k, last_q, n_vertical, n_slash, block),
+                    dev, workspace)
+    st = lib.vs_index_build(_ptr(q), _ptr(k), ctypes.byref(shape), ctypes.byref(cfg),
+                            _ptr(out["vertical"]), _ptr(out["slash"]), _ptr(out["blk_cnt"]),
+                            _ptr(out["blk_idx"]), _ptr(out["col_cnt"]), _ptr(out["col_idx"]),
+                            ctypes.byref(dbg) if dbg else None, _ptr(ws),
+                            ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check("vs_index_build", st)
+    return out
+
+
+def sparse_attn_prefill(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx, *, scale=None,
+                        block: int = 64, out=None, lse=None, want_lse: bool = True, stream=None):
+    """Causal attention over the listed tiles and columns; returns (out, lse or None)."""
+    lib = load()
+    _need_cuda(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx)
+    shape = prefill_shape(q, k)
+    if scale is None:
+        scale = shape.D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(shape.B, shape.H_q, shape.S, dtype=torch.float32, device=q.device)
+    st = lib.sparse_attn_prefill(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shape), block,
+                                 blk_idx.shape[-1], col_idx.shape[-1], _ptr(blk_cnt),
+                                 _ptr(blk_idx), _ptr(col_cnt), _ptr(col_idx),
+                                 ctypes.c_float(scale), _ptr(out), _ptr(lse), _stream(stream))
+    _check("sparse_attn_prefill", st)
+    return out, lse

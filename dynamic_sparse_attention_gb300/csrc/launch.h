@@ -1,0 +1,97 @@
+// Internal launcher interface between the C-ABI layer (api.cpp) and the kernels.
+// Arguments are validated by the caller; launchers only enqueue work.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace dsa {
+
+// One pruning stage's chunk scoring (SelectRep tournament + max over heads).
+struct StageScoreArgs {
+  const void *q;          // [B, T_q, H_q, D]
+  const void *k;          // [B, T_max, H_kv, D]
+  const int32_t *kv_len;  // [B]
+  int B, T_max, T_q, H_q, H_kv, D, dtype;
+  int n_sink, n_stream;   // stage 0 (implicit candidate range) only
+  const int32_t *in_idx;  // explicit input list [B, in_stride] (NULL for stage 0)
+  const int32_t *in_cnt;  // [B]
+  int in_stride;
+  int L;                  // chunk size
+  int max_chunks;         // row stride of score / rep arrays
+  float *score;           // [B, max_chunks]
+  int32_t *dbg_rep;       // [B, H_q, max_chunks] or NULL
+  float *dbg_rho;         // [B, H_q, max_chunks] or NULL
+};
+cudaError_t launch_stage_score(const StageScoreArgs &a, cudaStream_t s);
+
+// Top-K chunks + assembly of the kept tokens.
+struct StageTopkArgs {
+  const int32_t *kv_len;
+  int B, T_max;
+  int n_sink, n_stream;
+  const int32_t *in_idx;  // NULL for stage 0
+  const int32_t *in_cnt;
+  int in_stride;
+  int L, K;               // chunk size, chunks kept
+  int max_chunks;
+  const float *score;     // [B, max_chunks]
+  int32_t *out_idx;       // [B, out_stride]
+  int32_t *out_cnt;       // [B]
+  int out_stride;         // >= K * L
+  int32_t *dbg_idx;       // optional copy of out_idx (stride out_stride)
+  int32_t *dbg_cnt;
+};
+cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s);
+
+// Split-K decode over sink + selected + window keys, then the LSE merge.
+struct DecodeArgs {
+  const void *q, *k, *v;
+  const int32_t *kv_len;
+  const int32_t *sel_idx;
+  const int32_t *sel_cnt;
+  int max_sel, n_sink, n_stream;
+  float scale;
+  int B, T_max, T_q, H_q, H_kv, D, dtype;
+  int n_split, keys_per_split;
+  float *part;            // [B, n_split, T_q, H_q, D + 2]
+  void *out;
+  float *lse;
+};
+cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+
+// Decode split plan shared by the workspace query and the launch.
+void decode_plan(int B, int H_kv, int a_max, int *n_split, int *keys_per_split);
+
+// Vertical-slash index build.
+struct VsArgs {
+  const void *q, *k;
+  int B, S, H_q, H_kv, D;
+  int last_q, n_vertical, n_slash;
+  float scale;
+  int32_t *vertical, *slash, *blk_cnt, *blk_idx, *col_cnt, *col_idx;
+  float *dbg_vsum, *dbg_ssum;
+  // scratch
+  float *row_m, *row_l;       // [B, H_q, last_q] final row max / sum (base-2 logits)
+  float *part_m, *part_l;     // [B, H_kv, n_ktile, G*last_q] per key-tile stats
+  float *vsum, *ssum;         // [B, H_q, S]
+  float *slash_part;          // [B, H_q, n_ktile, KT + last_q - 1]
+  int n_ktile;
+};
+cudaError_t launch_vs_index(const VsArgs &a, cudaStream_t s);
+constexpr int kVsKeyTile = 64;
+
+// Sparse prefill attention over tile / column lists.
+struct PrefillArgs {
+  const void *q, *k, *v;
+  int B, S, H_q, H_kv, D;
+  int max_blk, max_col;
+  const int32_t *blk_cnt, *blk_idx, *col_cnt, *col_idx;
+  float scale;
+  void *out;
+  float *lse;
+};
+cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
+
+}  // namespace dsa

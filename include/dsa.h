@@ -1,0 +1,218 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) dynamic sparse attention library (libdsa.so).
+ *
+ * Two halves of one hot path:
+ *   decode : hip_select          -- InfiniteHiP hierarchical chunk pruning
+ *            sparse_attn_decode  -- split-K online-softmax GQA decode over the
+ *                                   sink + selected + window keys, with a merge
+ *   prefill: vs_index_build      -- MInference vertical-slash estimate, top-k and
+ *                                   conversion to per-query-block tile/column lists
+ *            sparse_attn_prefill -- causal attention over those 64x64 tiles and
+ *                                   gathered columns
+ *
+ * Conventions shared by every entry point
+ *   - Tensor arguments are DEVICE pointers owned by the caller.  Layouts are
+ *     row-major and contiguous ("bshd": batch, sequence, head, head-dim).
+ *     q, k, v and out must be 16-byte aligned; int32/float arrays 4-byte aligned.
+ *   - The library never allocates device memory and never synchronises.  Every
+ *     call enqueues its kernels on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) and returns at once.  Scratch memory, where needed, is the
+ *     caller's `ws` buffer, whose size the matching *_workspace() call returns.
+ *     Calls hold no state between them; two calls may run concurrently on
+ *     different streams if their ws and output buffers differ.
+ *   - No host synchronisation and fixed-size outputs: a decode step can be
+ *     captured in a CUDA graph.
+ *   - Return value: DSA_OK or a negative dsa_status.  On a validation failure
+ *     nothing is launched and no output is touched; dsa_last_error() gives a
+ *     message (thread-local).  DSA_ERR_CUDA reports a launch failure.
+ *   - Device-side data (kv_len, counts, index lists) is not read by the host.
+ *     Out-of-range values are clamped in the kernels (kv_len to [0, T_max],
+ *     counts to [0, capacity]); index entries must be valid positions.
+ */
+#ifndef DSA_H_
+#define DSA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_VERSION 1
+#define DSA_MAX_STAGES 8
+
+typedef enum {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = -1,  /* a shape, config or size is out of range */
+  DSA_ERR_UNSUPPORTED = -2,  /* valid, but not built (dtype, head dim, block size) */
+  DSA_ERR_WORKSPACE = -3,    /* ws missing or ws_bytes below the *_workspace() size */
+  DSA_ERR_ALIGNMENT = -4,    /* a pointer is NULL or misaligned */
+  DSA_ERR_CUDA = -5,         /* a kernel launch failed (message from the CUDA runtime) */
+  DSA_ERR_DEVICE_CHECK = -6  /* reserved for device-side checks */
+} dsa_status;
+
+typedef enum { DSA_BF16 = 0, DSA_F32 = 1 } dsa_dtype;
+
+/* ------------------------------------------------------------------ decode */
+
+/* Shape of one batched decode step.
+ *   q      [B, T_q, H_q, D]   the query block (T_q rows share one index set)
+ *   k, v   [B, T_max, H_kv, D] the resident KV cache; row t of batch b is valid
+ *                              for t < kv_len[b]
+ * H_q % H_kv == 0; query head h reads KV head h / (H_q / H_kv).
+ * D in {64, 128}; dtype DSA_BF16 (raw bf16) or DSA_F32. */
+typedef struct {
+  int B, T_max, T_q, H_q, H_kv, D;
+  int dtype;
+} dsa_decode_shape;
+
+/* Pruning configuration: n_stages stages, stage i with chunk size l_c = chunk[i]
+ * and token budget k = keep[i] (so it keeps K = keep[i] / chunk[i] chunks).
+ * 1 <= chunk[i] <= 4096, chunk[i] <= keep[i], keep non-increasing,
+ * keep[i] / chunk[i] <= 16384.  n_sink initial and n_stream newest tokens are
+ * never pruned and are attended by sparse_attn_decode. */
+typedef struct {
+  int n_stages;
+  int chunk[DSA_MAX_STAGES];
+  int keep[DSA_MAX_STAGES];
+  int n_sink, n_stream;
+} dsa_hip_cfg;
+
+/* Optional per-stage outputs for inspection; any pointer may be NULL.
+ *   stage_idx[i]  [B, keep[i]]             token list after stage i, ascending, -1 padded
+ *   stage_cnt[i]  [B]                      its length
+ *   chunk_score[i][B, dsa_hip_max_chunks(i)] chunk scores s_j (fp32)
+ *   rep[i]        [B, H_q, max_chunks(i)]  representative token of (head, chunk)
+ *   rep_score[i]  [B, H_q, max_chunks(i)]  its score max_t q_t . k_rep (fp32)
+ * Entries past a row's chunk count are left untouched. */
+typedef struct {
+  int32_t *stage_idx[DSA_MAX_STAGES];
+  int32_t *stage_cnt[DSA_MAX_STAGES];
+  float *chunk_score[DSA_MAX_STAGES];
+  int32_t *rep[DSA_MAX_STAGES];
+  float *rep_score[DSA_MAX_STAGES];
+} dsa_hip_debug;
+
+/* Upper bound on the chunk count of stage `stage` (host only). */
+int dsa_hip_max_chunks(const dsa_decode_shape *shape, const dsa_hip_cfg *cfg, int stage,
+                       int *n_chunks);
+
+/* Bytes of scratch hip_select needs for this shape and config (host only). */
+int hip_select_workspace(const dsa_decode_shape *shape, const dsa_hip_cfg *cfg, size_t *bytes);
+
+/* hip_select -- hierarchical chunk pruning of the middle tokens.
+ * Source: InfiniteHiP summary (arXiv 2502.08910), section 3.4, "Formal Mechanism
+ * of a Single Pruning Stage" (Alg. 2), "The Representative Token Selection
+ * Algorithm (SelectRep)" (Alg. 3), Alg. 1 line 1 (candidate range).
+ * For every batch row b with T = kv_len[b]:
+ *   I0 = [n_sink, T - n_stream); for each stage: split I into chunks of l_c,
+ *   pick a representative per (query head, chunk) by the halving tournament
+ *   (right half wins only on a strictly larger first-token score), score the
+ *   chunk by the max over heads and query rows of q . k_rep (fp32 dot of the
+ *   stored inputs), keep the K best chunks (ties -> smaller chunk index; all if
+ *   there are at most K), and concatenate their tokens in ascending order.
+ * Outputs: sel_idx [B, keep[n_stages-1]] final token list ascending, -1 padded;
+ *          sel_cnt [B] its length.  dbg may be NULL.
+ * Errors: INVALID_ARG / UNSUPPORTED for shapes and configs, ALIGNMENT for
+ * NULL/misaligned pointers, WORKSPACE if ws_bytes is short, CUDA on launch. */
+int hip_select(const void *q, const void *k, const int32_t *kv_len,
+               const dsa_decode_shape *shape, const dsa_hip_cfg *cfg,
+               int32_t *sel_idx, int32_t *sel_cnt, const dsa_hip_debug *dbg,
+               void *ws, size_t ws_bytes, void *stream);
+
+/* Bytes of scratch sparse_attn_decode needs (split-K partials) (host only). */
+int sparse_attn_decode_workspace(const dsa_decode_shape *shape, int max_sel, int n_sink,
+                                 int n_stream, size_t *bytes);
+
+/* sparse_attn_decode -- Flash-Decoding over the attended set of each row:
+ *   A = [0, min(n_sink,T)) U sel_idx[b, 0:sel_cnt[b]] U [max(n_sink, T-n_stream), T)
+ * out[b,t,h,:] = softmax_j(scale * q[b,t,h] . k[b,j,g]) v[b,j,g] over j in A,
+ * lse[b,t,h] = natural-log sum of exp(scale * q . k) (NULL to skip).
+ * Source: InfiniteHiP summary, section 3.4 "Block Sparse Attention
+ * Implementation" (Flash Decoding with a final reduction) and "Formal
+ * Background" (softmax attention); InfLLM guide, "Chunk-Level Attention Scoring
+ * Engine" (softmax over sink U retrieved U local keys with 1/sqrt(d_k)).
+ * sel_idx [B, max_sel] int32, entries ascending and inside [n_sink, T-n_stream);
+ * sel_cnt [B] (clamped to [0, max_sel]).  out has the dtype of q.  A row with an
+ * empty A gets out = 0 and lse = -inf.
+ * Errors as for hip_select. */
+int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_t *kv_len,
+                       const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, int n_sink,
+                       int n_stream, float scale, const dsa_decode_shape *shape, void *out,
+                       float *lse, void *ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------ prefill */
+
+/* Shape of one causal prefill: q/out [B, S, H_q, D], k/v [B, S, H_kv, D], bf16,
+ * D in {64, 128}, H_q % H_kv == 0. */
+typedef struct {
+  int B, S, H_q, H_kv, D;
+} dsa_prefill_shape;
+
+/* Vertical-slash budgets: last_q estimate rows (<= 64 used: min(last_q, S)),
+ * n_vertical columns and n_slash offsets kept per head (each <= S, >= 0),
+ * tile size `block` (64 only). */
+typedef struct {
+  int last_q, n_vertical, n_slash, block;
+} dsa_vs_cfg;
+
+/* Optional estimate sums for inspection (NULL allowed): vsum / ssum [B, H_q, S]
+ * fp32 column sums and slash (diagonal) sums of the estimated attention. */
+typedef struct {
+  float *vsum;
+  float *ssum;
+} dsa_vs_debug;
+
+int vs_index_build_workspace(const dsa_prefill_shape *shape, const dsa_vs_cfg *cfg,
+                             size_t *bytes);
+
+/* vs_index_build -- MInference vertical-slash index for every (b, query head).
+ * Source: MInference summary (arXiv 2407.02490), section 3.4 "Online Dynamic
+ * Index Estimation: Vertical-Slash Heads" (Alg. 2 steps 1-4) and "Vertical-Slash
+ * Hybrid Kernel" (Alg. 4, two-way merge).
+ *   A~ = softmax(q[S-r:S] k^T / sqrt(D) + causal) for the r = min(last_q, S) last
+ *   queries; vertical = top n_vertical column sums, slash = top n_slash diagonal
+ *   sums (offset o = query pos - key pos), ties -> smaller index, both ascending.
+ *   Conversion, per query block m (nominal rows 64m..64m+63): the key blocks that
+ *   the slash segments [64m-o, 64m+63-o] touch (clipped at 0) form the block
+ *   list; vertical columns <= 64m+63 outside those blocks form the column list.
+ * Outputs (n_qblk = ceil(S/64)):
+ *   vertical [B, H_q, n_vertical], slash [B, H_q, n_slash]   ascending
+ *   blk_cnt [B, H_q, n_qblk], blk_idx [B, H_q, n_qblk, n_qblk] ascending key blocks
+ *   col_cnt [B, H_q, n_qblk], col_idx [B, H_q, n_qblk, n_vertical] ascending keys
+ * Unused tails of blk_idx / col_idx rows are left untouched.  dbg may be NULL. */
+int vs_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
+                   const dsa_vs_cfg *cfg, int32_t *vertical, int32_t *slash, int32_t *blk_cnt,
+                   int32_t *blk_idx, int32_t *col_cnt, int32_t *col_idx,
+                   const dsa_vs_debug *dbg, void *ws, size_t ws_bytes, void *stream);
+
+/* sparse_attn_prefill -- causal attention of each query block over its listed
+ * 64x64 key tiles, then its listed columns gathered 64 at a time, with one
+ * online softmax.  Source: MInference summary, "Vertical-Slash Hybrid Kernel"
+ * (Alg. 5) and "Block-Sparse FlashAttention Kernel (Appendix C.4.1)"; masked
+ * attention of section 3.4 Eq. 1 with the mask constant as exact exclusion.
+ * Row i of query block m attends key j <= i iff floor(j/64) is in
+ * blk_idx[b,h,m,0:blk_cnt] or j is in col_idx[b,h,m,0:col_cnt].
+ *   blk_idx [B, H_q, n_qblk, max_blk]  key-block ids, each < n_qblk, distinct
+ *   col_idx [B, H_q, n_qblk, max_col]  key positions < S, distinct, not inside a
+ *                                      listed block (else counted twice)
+ * out [B, S, H_q, D] bf16; lse [B, H_q, S] fp32 natural log (NULL to skip).
+ * A row with no attended key gets out = 0, lse = -inf.  block must be 64. */
+int sparse_attn_prefill(const void *q, const void *k, const void *v,
+                        const dsa_prefill_shape *shape, int block, int max_blk, int max_col,
+                        const int32_t *blk_cnt, const int32_t *blk_idx, const int32_t *col_cnt,
+                        const int32_t *col_idx, float scale, void *out, float *lse,
+                        void *stream);
+
+/* ------------------------------------------------------------------ helpers */
+
+const char *dsa_last_error(void);   /* last validation / launch message of this thread */
+const char *dsa_strerror(int status);
+int dsa_version(void);              /* DSA_VERSION */
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DSA_H_ */

@@ -1,0 +1,110 @@
+"""The C-ABI library builds, loads, exports every declared symbol and validates
+its arguments on the host (no GPU needed: every call here fails before any launch)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from dynamic_sparse_attention_gb300 import _build, binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return binding.load()
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(\w+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_four_entry_points():
+    names = _declared()
+    for n in ("hip_select", "sparse_attn_decode", "vs_index_build", "sparse_attn_prefill"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared() if not hasattr(lib, n)]
+    assert not missing, f"declared in include/dsa.h but not exported: {missing}"
+
+
+def test_version_and_strerror(lib):
+    assert lib.dsa_version() == 1
+    assert lib.dsa_strerror(-3) == b"workspace missing or too small"
+
+
+def _shape(**kw):
+    d = dict(B=1, T_max=4096, T_q=1, H_q=32, H_kv=8, D=128, dtype=0)
+    d.update(kw)
+    return binding.DecodeShape(**d)
+
+
+def _cfg(chunk=(256, 64, 16, 4), keep=(2048, 1024, 512, 256), n_sink=16, n_stream=64):
+    return binding.HipConfig(chunk, keep, n_sink, n_stream).c()
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(H_q=30), -1), (dict(D=96), -2), (dict(dtype=5), -2), (dict(B=0), -1),
+    (dict(T_q=0), -1), (dict(H_q=256, H_kv=8), -2),
+])
+def test_bad_shapes_rejected(lib, kw, status):
+    n = ctypes.c_size_t()
+    s = _shape(**kw)
+    c = _cfg()
+    assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == status
+    assert lib.dsa_last_error()
+
+
+@pytest.mark.parametrize("chunk,keep", [
+    ((0,), (16,)), ((64,), (32,)), ((16, 16), (64, 128)), ((8192,), (8192,)),
+])
+def test_bad_configs_rejected(lib, chunk, keep):
+    n = ctypes.c_size_t()
+    s = _shape()
+    c = _cfg(chunk, keep)
+    assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == -1
+
+
+def test_workspace_sizes(lib):
+    n = ctypes.c_size_t()
+    s = _shape(T_max=1 << 20)
+    c = _cfg(keep=(32768, 16384, 8192, 4096), n_sink=128, n_stream=1024)
+    assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == 0
+    # scores for every stage + lists for the first three stages
+    assert n.value >= 4 * (4092 + 512 + 1024 + 2048) + 4 * (32768 + 16384 + 8192)
+    m = ctypes.c_int()
+    assert lib.dsa_hip_max_chunks(ctypes.byref(s), ctypes.byref(c), 0, ctypes.byref(m)) == 0
+    assert m.value == (1048576 - 128 - 1024 + 255) // 256
+    assert lib.sparse_attn_decode_workspace(ctypes.byref(s), 4096, 128, 1024, ctypes.byref(n)) == 0
+    assert n.value > 0
+
+
+def test_null_and_misaligned_pointers_rejected(lib):
+    s = _shape()
+    c = _cfg()
+    buf = (ctypes.c_char * 64)()
+    base = ctypes.addressof(buf)
+    mis = ctypes.c_void_p(base + (1 if base % 16 else 2))
+    ok = ctypes.c_void_p(base + (-base % 16))
+    null = ctypes.c_void_p(0)
+    # q NULL
+    st = lib.hip_select(null, ok, ok, ctypes.byref(s), ctypes.byref(c), ok, ok, None, ok,
+                        ctypes.c_size_t(1 << 30), None)
+    assert st == -4
+    # q misaligned
+    st = lib.hip_select(mis, ok, ok, ctypes.byref(s), ctypes.byref(c), ok, ok, None, ok,
+                        ctypes.c_size_t(1 << 30), None)
+    assert st == -4
+    # workspace too small
+    st = lib.hip_select(ok, ok, ok, ctypes.byref(s), ctypes.byref(c), ok, ok, None, ok,
+                        ctypes.c_size_t(8), None)
+    assert st == -3
+    st = lib.sparse_attn_decode(ok, ok, ok, ok, ok, ok, 16, 4, 4, ctypes.c_float(float("nan")),
+                                ctypes.byref(s), ok, None, ok, ctypes.c_size_t(1 << 30), None)
+    assert st == -1

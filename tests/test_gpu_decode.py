@@ -1,0 +1,131 @@
+"""GPU parity of the decode half (hip_select + sparse_attn_decode) against the fp64 oracle."""
+import numpy as np
+import pytest
+import torch
+
+import dynamic_sparse_attention_gb300 as dsa
+from dynamic_sparse_attention_gb300 import _build
+from oracle import hip
+from oracle.numerics import to_f64
+from parity import attention_errors, check_hip_row, from_dev_bits, to_dev
+from synth import decode_128k, decode_batch16, decode_case, decode_tiny
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS, MEAN_ABS = 1e-2, 1e-3
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    _build.build()
+    dsa.load()
+
+
+def _run(case):
+    q = to_dev(case.q, case.dtype)
+    k = to_dev(case.k, case.dtype)
+    v = to_dev(case.v, case.dtype)
+    kv_len = torch.from_numpy(case.kv_len).cuda()
+    cfg = dsa.HipConfig(case.chunk, case.keep, case.n_sink, case.n_stream)
+    sel_idx, sel_cnt, dbg = dsa.hip_select(q, k, kv_len, cfg, debug=True)
+    out, lse = dsa.sparse_attn_decode(q, k, v, kv_len, sel_idx, sel_cnt, n_sink=case.n_sink,
+                                      n_stream=case.n_stream)
+    torch.cuda.synchronize()
+    return sel_idx, sel_cnt, dbg, out, lse
+
+
+def _check_case(case, rows=None):
+    sel_idx, sel_cnt, dbg, out, lse = _run(case)
+    o_gpu = from_dev_bits(out)
+    if case.dtype == "bf16":
+        o_gpu = to_f64(o_gpu, "bf16")
+    lse_gpu = lse.cpu().numpy()
+    report = []
+    for b in (range(case.B) if rows is None else rows):
+        I, stats = check_hip_row(case, b, dbg, sel_idx, sel_cnt)
+        T = int(case.kv_len[b])
+        A = hip.attended_set(T, case.n_sink, case.n_stream, I)
+        q64 = to_f64(case.q[b], case.dtype)
+        O64, lse64 = hip.decode_attention(q64, case.k[b], case.v[b], case.dtype, A, case.scale,
+                                          case.G)
+        mx, mn = attention_errors(o_gpu[b], O64)
+        assert mx <= MAX_ABS and mn <= MEAN_ABS, f"row {b}: max {mx:.3e} mean {mn:.3e}"
+        fin = np.isfinite(lse64)
+        assert np.array_equal(fin, np.isfinite(lse_gpu[b]))
+        assert np.abs(lse_gpu[b][fin] - lse64[fin]).max(initial=0) <= 1e-3
+        report.append((b, stats, mx, mn))
+    return report
+
+
+def test_tiny_fp32_config():
+    """1 head, d=64, fp32, 32 query rows, 64->16->4 chunks (the small oracle case)."""
+    _check_case(decode_tiny())
+
+
+@pytest.mark.parametrize("D,dtype", [(64, "bf16"), (128, "bf16"), (128, "f32"), (64, "f32")])
+def test_gqa_small_ragged(D, dtype):
+    """GQA, ragged batch lengths, partial last chunks, several tiles and splits."""
+    c = decode_case("ragged", B=3, T=5000, T_q=1, H_q=8, H_kv=2, D=D, dtype=dtype,
+                    chunk=(64, 16, 4), keep=(1024, 256, 64), n_sink=13, n_stream=100, seed=31,
+                    plant="uniform", n_plant=16, kv_len=[5000, 3333, 1210])
+    _check_case(c)
+
+
+def test_multi_row_query_block():
+    c = decode_case("block", B=2, T=3000, T_q=4, H_q=4, H_kv=1, D=128, dtype="bf16",
+                    chunk=(32, 8), keep=(512, 128), n_sink=8, n_stream=32, seed=32,
+                    plant="none", kv_len=[3000, 2001])
+    _check_case(c)
+
+
+def test_edge_cases_short_contexts():
+    """Contexts shorter than sink + window, empty candidate ranges, keep-all stages."""
+    c = decode_case("short", B=4, T=700, T_q=1, H_q=4, H_kv=4, D=64, dtype="bf16",
+                    chunk=(16, 4), keep=(4096, 64), n_sink=32, n_stream=64, seed=33,
+                    plant="none", kv_len=[700, 96, 50, 97])
+    _check_case(c)
+
+
+def test_non_power_of_two_chunks():
+    c = decode_case("odd", B=1, T=4000, T_q=2, H_q=6, H_kv=3, D=64, dtype="f32",
+                    chunk=(100, 13, 3), keep=(1300, 390, 90), n_sink=5, n_stream=21, seed=34,
+                    plant="none")
+    _check_case(c)
+
+
+def test_dense_keep_all_matches_sdpa():
+    c = decode_case("dense", B=2, T=1500, T_q=1, H_q=8, H_kv=2, D=128, dtype="bf16",
+                    chunk=(64, 16), keep=(1 << 14, 1 << 14), n_sink=4, n_stream=16, seed=35,
+                    plant="none")
+    sel_idx, sel_cnt, dbg, out, lse = _run(c)
+    assert np.array_equal(sel_cnt.cpu().numpy(), [1500 - 20] * 2)
+    qt = to_dev(c.q, "bf16").float().permute(0, 2, 1, 3)
+    kt = to_dev(c.k, "bf16").float().permute(0, 2, 1, 3).repeat_interleave(4, 1)
+    vt = to_dev(c.v, "bf16").float().permute(0, 2, 1, 3).repeat_interleave(4, 1)
+    ref = torch.nn.functional.scaled_dot_product_attention(qt, kt, vt).permute(0, 2, 1, 3)
+    assert (out.float() - ref).abs().max().item() <= MAX_ABS
+
+
+def test_value_shift_metamorphic():
+    c = decode_case("shift", B=1, T=3000, T_q=1, H_q=8, H_kv=2, D=128, dtype="f32",
+                    chunk=(64, 8), keep=(512, 128), n_sink=8, n_stream=64, seed=36)
+    q, k, v = to_dev(c.q, "f32"), to_dev(c.k, "f32"), to_dev(c.v, "f32")
+    kv_len = torch.from_numpy(c.kv_len).cuda()
+    cfg = dsa.HipConfig(c.chunk, c.keep, c.n_sink, c.n_stream)
+    sel_idx, sel_cnt = dsa.hip_select(q, k, kv_len, cfg)
+    o1, _ = dsa.sparse_attn_decode(q, k, v, kv_len, sel_idx, sel_cnt, n_sink=8, n_stream=64)
+    o2, _ = dsa.sparse_attn_decode(q, k, v + 0.5, kv_len, sel_idx, sel_cnt, n_sink=8, n_stream=64)
+    sel2, cnt2 = dsa.hip_select(q * 2.0, k, kv_len, cfg)  # exact scaling: same decisions
+    assert torch.equal(sel_idx, sel2) and torch.equal(sel_cnt, cnt2)
+    assert (o2 - o1 - 0.5).abs().max().item() < 1e-5
+
+
+def test_gqa_128k_config():
+    """Llama-3-8B-shaped GQA decode at context 131072 (full size, replay parity)."""
+    _check_case(decode_128k())
+
+
+def test_batch16_config():
+    """Batch 16 at 32K with one planted cluster per row (checks rows 0, 7 and 15 in full)."""
+    _check_case(decode_batch16(), rows=[0, 7, 15])
