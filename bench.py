@@ -1,0 +1,581 @@
+#!/usr/bin/env python
+"""Benchmark of the sparse-attention hot path on GB300.
+
+One step = one pass of the whole hot path on synthetic input:
+  decode : hip_select (4 pruning stages) + sparse_attn_decode at context 1,048,576
+           (32 query / 8 KV heads, d=128, bf16, keep 32768/16384/8192/4096, sink 128,
+           window 1024, full re-selection every step);
+  prefill: vs_index_build + sparse_attn_prefill at S=131072 (32/8 heads, d=128, bf16,
+           top 1000 vertical / 6096 slash, 64x64 tiles).
+The printed line carries decode us/step (the headline `value`, CUDA-graph replay),
+prefill ms, the roofline of each half's dominant kernel (CUDA-event durations of
+that kernel inside the run), an end-to-end number through the public API with
+host buffers, SM clocks sampled during the timed region, and the fp64 oracle
+timed on the host cores.  `--impl reference` times the oracle alone.
+
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run every rank runs its own replica (weak scaling).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn decode μs/step @1M ctx; prefill ms @128K; % HBM / TC roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def parse_args():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=10)
+    p.add_argument("--warmup", type=int, default=3)
+    p.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    p.add_argument("--no-cpu-baseline", action="store_true", help="skip the oracle leg")
+    p.add_argument("--small", action="store_true",
+                   help="small shapes (context 131072 decode, S=16384 prefill) for a quick check")
+    return p.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [x.strip() for x in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for name, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(name)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workloads
+
+def workloads(small: bool):
+    import synth
+    if small:
+        dec = synth.decode_case("decode_gqa_T131072", B=1, T=131072, T_q=1, H_q=32, H_kv=8,
+                                D=128, dtype="bf16", chunk=(256, 64, 16, 4),
+                                keep=(32768, 16384, 8192, 4096), n_sink=128, n_stream=1024,
+                                seed=1, plant="uniform", n_plant=64)
+        pre = synth.prefill_case("prefill_vs_S16384", S=16384, H_q=32, H_kv=8, D=128, seed=4)
+    else:
+        dec = synth.decode_1m()
+        pre = synth.prefill_128k()
+    return dec, pre
+
+
+def to_dev(a, torch, dev):
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).to(dev)
+
+
+# ------------------------------------------------------------------ oracle leg
+
+def oracle_decode_step(dec):
+    """The oracle's full decode step for batch row 0 (selection + attention); seconds."""
+    from oracle import hip
+    from oracle.numerics import to_f64
+    t0 = time.perf_counter()
+    q64 = to_f64(dec.q[0], dec.dtype)
+    T = int(dec.kv_len[0])
+    _, I = hip.hip_select(q64, dec.k[0], dec.dtype, T, dec.chunk, dec.keep, dec.n_sink,
+                          dec.n_stream, dec.G)
+    A = hip.attended_set(T, dec.n_sink, dec.n_stream, I)
+    hip.decode_attention(q64, dec.k[0], dec.v[0], dec.dtype, A, dec.scale, dec.G)
+    return time.perf_counter() - t0
+
+
+def oracle_prefill_sample(pre, n_heads=1, n_blocks=4):
+    """Oracle prefill on a bounded sample, extrapolated to the whole problem; ms.
+
+    Sample: the vertical-slash estimate and conversion of `n_heads` heads, and the
+    attention of `n_blocks` query blocks of head 0 spread over the sequence; the
+    estimate scales by heads, the attention by the number of listed tiles.
+    """
+    from oracle import vs
+    from oracle.numerics import to_f64
+    S, H_q = pre.S, pre.H_q
+    rows = vs.estimate_rows(S, pre.last_q)
+    t_est = 0.0
+    blk = col = None
+    for h in range(n_heads):
+        t0 = time.perf_counter()
+        g = h // pre.G
+        A = vs.approx_attention(to_f64(pre.q[0, rows, h], "bf16"), rows,
+                                to_f64(pre.k[0, :, g], "bf16"), pre.scale)
+        v = vs.vertical_sums(A)
+        s = vs.slash_sums(A, rows)
+        vert = vs.topk_ascending(v, pre.n_vertical)
+        sl = vs.topk_ascending(s, pre.n_slash)
+        blk, col = vs.vs_convert(vert, sl, S)
+        t_est += time.perf_counter() - t0
+    nq = len(blk)
+    tiles = [len(blk[m]) + -(-len(col[m]) // 64) for m in range(nq)]
+    sample = np.linspace(0, nq - 1, n_blocks).astype(int)
+    t0 = time.perf_counter()
+    for m in sample:
+        vs.prefill_block_attention(pre.q[0], pre.k[0], pre.v[0], 0, pre.G, int(m), blk[m], col[m],
+                                   S, pre.scale)
+    t_att = time.perf_counter() - t0
+    sample_tiles = sum(tiles[m] for m in sample)
+    total_ms = 1e3 * (t_est * H_q / n_heads + t_att * (sum(tiles) * H_q) / max(1, sample_tiles))
+    desc = (f"estimate+convert of {n_heads}/{H_q} heads (x{H_q // n_heads}), attention of "
+            f"{n_blocks} query blocks of head 0 ({sample_tiles} of {sum(tiles) * H_q} tiles, "
+            f"extrapolated by tile count)")
+    return total_ms, desc
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_model():
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def cpu_baseline(dec, pre):
+    dec_s = oracle_decode_step(dec)
+    pre_ms, pre_desc = oracle_prefill_sample(pre)
+    return {
+        "value": dec_s * 1e6, "unit": "us/step", "cores": host_cores(), "kind": "oracle",
+        "cpu": cpu_model(),
+        "sample": (f"decode: one full step of {dec.name} (selection + attention, batch row 0); "
+                   f"prefill: {pre_desc}"),
+        "prefill_ms_extrapolated": pre_ms,
+    }
+
+
+def run_reference(args, rank):
+    """The oracle as it stands on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    dec, pre = workloads(args.small)
+    for _ in range(args.warmup):
+        oracle_decode_step(dec)
+    times, pre_ms = [], []
+    for _ in range(args.steps):
+        times.append(oracle_decode_step(dec) * 1e6)
+    pre_ms_val, pre_desc = oracle_prefill_sample(pre)
+    v = statistics.mean(times)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": v, "unit": "us/step",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": v / 1e3 + pre_ms_val, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{dec.name} + {pre.name}", "parallelism": "single process, host cores"},
+        "prefill": {"ms": pre_ms_val, "sample": pre_desc},
+        "cpu_baseline": {"value": v, "unit": "us/step", "cores": host_cores(), "kind": "oracle",
+                         "cpu": cpu_model(),
+                         "sample": f"decode: full step of {dec.name}, batch row 0; prefill: {pre_desc}"},
+        "e2e": {"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU leg
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        run_reference(args, rank)
+        return
+
+    import torch
+    import dynamic_sparse_attention_gb300 as dsa
+    from dynamic_sparse_attention_gb300 import accounting
+    import torch.distributed as dist
+
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    dsa.load()
+    peaks, peaks_src = load_peaks()
+
+    dec, pre = workloads(args.small)
+    # ---------------- decode buffers (resident)
+    q = to_dev(dec.q, torch, dev)
+    k = to_dev(dec.k, torch, dev)
+    v = to_dev(dec.v, torch, dev)
+    kv_len = torch.from_numpy(dec.kv_len).to(dev)
+    cfg = dsa.HipConfig(dec.chunk, dec.keep, dec.n_sink, dec.n_stream)
+    sel_idx = torch.empty(dec.B, dec.keep[-1], dtype=torch.int32, device=dev)
+    sel_cnt = torch.empty(dec.B, dtype=torch.int32, device=dev)
+    ws_sel = torch.empty(dsa.hip_select_workspace_bytes(q, k, cfg), dtype=torch.uint8, device=dev)
+    ws_dec = torch.empty(max(1, dsa.sparse_attn_decode_workspace_bytes(q, k, dec.keep[-1], dec.n_sink,
+                                                                       dec.n_stream)),
+                         dtype=torch.uint8, device=dev)
+    out = torch.empty_like(q)
+    lse = torch.empty(dec.B, dec.T_q, dec.H_q, dtype=torch.float32, device=dev)
+
+    def decode_step():
+        dsa.hip_select(q, k, kv_len, cfg, out=(sel_idx, sel_cnt), workspace=ws_sel)
+        dsa.sparse_attn_decode(q, k, v, kv_len, sel_idx, sel_cnt, n_sink=dec.n_sink,
+                               n_stream=dec.n_stream, out=out, lse=lse, workspace=ws_dec)
+
+    # ---------------- prefill buffers (resident)
+    pq, pk, pv = to_dev(pre.q, torch, dev), to_dev(pre.k, torch, dev), to_dev(pre.v, torch, dev)
+    nq = (pre.S + 63) // 64
+    idx = {
+        "vertical": torch.empty(1, pre.H_q, pre.n_vertical, dtype=torch.int32, device=dev),
+        "slash": torch.empty(1, pre.H_q, pre.n_slash, dtype=torch.int32, device=dev),
+        "blk_cnt": torch.empty(1, pre.H_q, nq, dtype=torch.int32, device=dev),
+        "blk_idx": torch.empty(1, pre.H_q, nq, nq, dtype=torch.int32, device=dev),
+        "col_cnt": torch.empty(1, pre.H_q, nq, dtype=torch.int32, device=dev),
+        "col_idx": torch.empty(1, pre.H_q, nq, pre.n_vertical, dtype=torch.int32, device=dev),
+    }
+    ws_vs = torch.empty(dsa.vs_index_build_workspace_bytes(pq, pk, pre.last_q, pre.n_vertical,
+                                                           pre.n_slash), dtype=torch.uint8, device=dev)
+    pout = torch.empty_like(pq)
+    plse = torch.empty(1, pre.H_q, pre.S, dtype=torch.float32, device=dev)
+
+    def prefill_index():
+        dsa.vs_index_build(pq, pk, last_q=pre.last_q, n_vertical=pre.n_vertical,
+                           n_slash=pre.n_slash, out=idx, workspace=ws_vs)
+
+    def prefill_attn():
+        dsa.sparse_attn_prefill(pq, pk, pv, idx["blk_cnt"], idx["blk_idx"], idx["col_cnt"],
+                                idx["col_idx"], out=pout, lse=plse)
+
+    flush_buf = torch.empty(512 << 20, dtype=torch.uint8, device=dev)
+
+    def flush():
+        flush_buf.fill_(1)
+
+    ev = lambda: torch.cuda.Event(enable_timing=True)  # noqa: E731
+
+    # ---------------- warm-up (eager), then capture the decode step
+    for _ in range(max(3, args.warmup)):
+        decode_step()
+        prefill_index()
+        prefill_attn()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        decode_step()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        decode_step()
+    for _ in range(3):
+        graph.replay()
+    torch.cuda.synchronize()
+
+    # ---------------- timed region
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    dec_ms, idx_ms, att_ms = [], [], []
+    barrier()
+    with ClockSampler(local_rank) as clocks:
+        for _ in range(args.steps):
+            flush()
+            e0, e1 = ev(), ev()
+            e0.record()
+            graph.replay()
+            e1.record()
+            flush()
+            e2, e3, e4 = ev(), ev(), ev()
+            e2.record()
+            prefill_index()
+            e3.record()
+            prefill_attn()
+            e4.record()
+            dec_ms.append((e0, e1))
+            idx_ms.append((e2, e3))
+            att_ms.append((e3, e4))
+        barrier()
+    dec_ms = [a.elapsed_time(b) for a, b in dec_ms]
+    idx_ms = [a.elapsed_time(b) for a, b in idx_ms]
+    att_ms = [a.elapsed_time(b) for a, b in att_ms]
+    clock_info = clocks.summary()
+
+    # eager decode (same steps, for reference)
+    eager = []
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = ev(), ev()
+        e0.record()
+        decode_step()
+        e1.record()
+        eager.append((e0, e1))
+    torch.cuda.synchronize()
+    eager = [a.elapsed_time(b) for a, b in eager]
+
+    # ---------------- per-kernel durations (CUDA events on the launch stream)
+    dsa.profile_enable(True)
+    for _ in range(args.steps):
+        flush()
+        decode_step()
+        flush()
+        prefill_index()
+        prefill_attn()
+    torch.cuda.synchronize()
+    dsa.profile_enable(False)
+    kstats = dsa.profile_collect()
+    per_step_launches = sum(n for n, _ in kstats.values()) / args.steps
+    kern = {name: {"launches": n, "avg_us": 1e3 * t / n} for name, (n, t) in kstats.items()}
+
+    # ---------------- algorithmic work (from one debug run of the same inputs)
+    sel2, cnt2, dbg = dsa.hip_select(q, k, kv_len, cfg, debug=True)
+    torch.cuda.synchronize()
+    T = int(dec.kv_len[0])
+    elem = 2
+    prev = np.arange(dec.n_sink, max(dec.n_sink, T - dec.n_stream))
+    stage_bytes, stage_rows, stage_chunks = [], [], []
+    for i, L in enumerate(dec.chunk):
+        n = -(-len(prev) // L)
+        chunks = [prev[j * L:(j + 1) * L] for j in range(n)]
+        lens = np.array([len(c) for c in chunks], np.int64)
+        reps = dbg["rep"][i][0, :, :n].cpu().numpy().astype(np.int64)
+        rows = accounting.stage_rows(reps, None, chunks, lens, dec.G)
+        stage_rows.append(rows)
+        stage_chunks.append(n)
+        idx_bytes = 0 if i == 0 else 4 * len(prev)
+        stage_bytes.append(rows * dec.D * elem + idx_bytes + 4 * n + dec.T_q * dec.H_q * dec.D * elem)
+        cnt = int(dbg["stage_cnt"][i][0])
+        prev = dbg["stage_idx"][i][0, :cnt].cpu().numpy()
+    attended = min(dec.n_sink, T) + int(cnt2[0]) + (T - max(dec.n_sink, T - dec.n_stream))
+    attn_bytes = attended * dec.H_kv * dec.D * elem * 2 + 2 * dec.T_q * dec.H_q * dec.D * elem
+    step_bytes = sum(r * dec.D * elem for r in stage_rows) + attn_bytes
+    dec_kernel_bytes = {f"hip_stage_score_s{i}": b for i, b in enumerate(stage_bytes)}
+    dec_kernel_bytes["decode_splitk"] = attn_bytes
+    for name, b in dec_kernel_bytes.items():
+        if name in kern:
+            kern[name]["algorithmic_bytes"] = b
+            kern[name]["achieved_GBps"] = b / (kern[name]["avg_us"] * 1e-6) / 1e9
+
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    dec_names = [n for n in kern if n.startswith("hip_") or n.startswith("decode_")]
+    dom = max(dec_names, key=lambda n: kern[n]["avg_us"] * kern[n]["launches"])
+    dom_bytes = dec_kernel_bytes.get(dom)
+    achieved = dom_bytes / (kern[dom]["avg_us"] * 1e-6) / 1e9 if dom_bytes else None
+    roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
+                "frac": achieved / hbm if achieved else None, "traffic": None,
+                "peak_source": f"{peaks_src} hbm_gbs",
+                "algorithmic_bytes_per_launch": dom_bytes}
+
+    # prefill tiles and FLOPs
+    blk_cnt = idx["blk_cnt"].cpu().numpy()
+    col_cnt = idx["col_cnt"].cpu().numpy()
+    flops = accounting.prefill_tile_flops(blk_cnt, col_cnt, pre.D)
+    tiles = int(blk_cnt.sum() + np.ceil(col_cnt / 64.0).sum())
+    dense_tiles = accounting.causal_dense_tiles(pre.S) * pre.H_q
+    att_name = [n for n in kern if n.startswith("prefill_attention")][0]
+    att_us = kern[att_name]["avg_us"]
+    tc_peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    tflops = flops / (att_us * 1e-6) / 1e12
+    kern[att_name]["algorithmic_flops"] = flops
+    kern[att_name]["achieved_TFLOPs"] = tflops
+    vs_bytes = accounting.vs_index_bytes(1, pre.S, pre.H_q, pre.H_kv, pre.D, pre.n_vertical)
+    vs_us = sum(kern[n]["avg_us"] for n in kern if n.startswith("vs_"))
+    roofline_prefill = {"kernel": att_name, "bound": "tensor", "achieved": tflops, "peak": tc_peak,
+                        "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": None,
+                        "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                        "algorithmic_flops_per_launch": flops}
+
+    # ---------------- end to end through the public API with host buffers
+    h_q = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
+    h_q.copy_(q)
+    h_kn = torch.empty(k[:, T - 1].shape, dtype=k.dtype, pin_memory=True)
+    h_vn = torch.empty_like(h_kn, pin_memory=True)
+    h_kn.copy_(k[:, T - 1])
+    h_vn.copy_(v[:, T - 1])
+    h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    e2e = []
+    for _ in range(args.steps):
+        flush()
+        e0, e1 = ev(), ev()
+        e0.record()
+        q.copy_(h_q, non_blocking=True)
+        k[:, T - 1].copy_(h_kn, non_blocking=True)   # the newest token's key / value row
+        v[:, T - 1].copy_(h_vn, non_blocking=True)
+        decode_step()
+        h_out.copy_(out, non_blocking=True)
+        e1.record()
+        e2e.append((e0, e1))
+    torch.cuda.synchronize()
+    e2e = [a.elapsed_time(b) for a, b in e2e]
+    h2d = h_q.numel() * 2 + 2 * h_kn.numel() * 2
+    d2h = h_out.numel() * 2
+    hp = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (pq, pk, pv)]
+    for h_, d_ in zip(hp, (pq, pk, pv)):
+        h_.copy_(d_)
+    h_pout = torch.empty(pout.shape, dtype=pout.dtype, pin_memory=True)
+    pe2e = []
+    for _ in range(min(args.steps, 3)):
+        flush()
+        e0, e1 = ev(), ev()
+        e0.record()
+        for h_, d_ in zip(hp, (pq, pk, pv)):
+            d_.copy_(h_, non_blocking=True)
+        prefill_index()
+        prefill_attn()
+        h_pout.copy_(pout, non_blocking=True)
+        e1.record()
+        pe2e.append((e0, e1))
+    torch.cuda.synchronize()
+    pe2e = [a.elapsed_time(b) for a, b in pe2e]
+
+    # ---------------- max over ranks
+    dec_us = 1e3 * statistics.mean(dec_ms)
+    pre_ms = statistics.mean(idx_ms) + statistics.mean(att_ms)
+    if world > 1:
+        t = torch.tensor([dec_us, pre_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dec_us, pre_ms = float(t[0]), float(t[1])
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(dec, pre)
+
+    line = {
+        "metric": METRIC,
+        "value": dec_us,
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": dec_us / 1e3 + pre_ms,
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": f"{dec.name} + {pre.name}",
+            "decode": {"B": dec.B, "T": dec.T_max, "H_q": dec.H_q, "H_kv": dec.H_kv, "D": dec.D,
+                       "chunk": list(dec.chunk), "keep": list(dec.keep), "n_sink": dec.n_sink,
+                       "n_stream": dec.n_stream, "selection": "full re-selection every step"},
+            "prefill": {"S": pre.S, "H_q": pre.H_q, "H_kv": pre.H_kv, "D": pre.D,
+                        "last_q": pre.last_q, "n_vertical": pre.n_vertical, "n_slash": pre.n_slash},
+            "l2": "flushed (512 MiB write) before each timed decode step and prefill",
+            "parallelism": "replicas" if world > 1 else "single GPU",
+            "decode_timing": "CUDA graph replay of hip_select + sparse_attn_decode",
+        },
+        "decode": {
+            "us_per_step_graph": dec_us,
+            "us_per_step_eager": 1e3 * statistics.mean(eager),
+            "algorithmic_bytes_per_step": step_bytes,
+            "step_hbm_frac": step_bytes / (dec_us * 1e-6) / 1e9 / hbm,
+            "tournament_rows_per_stage": stage_rows,
+            "chunks_per_stage": stage_chunks,
+            "attended_keys": attended,
+        },
+        "prefill": {
+            "ms": pre_ms,
+            "vs_index_ms": statistics.mean(idx_ms),
+            "attention_ms": statistics.mean(att_ms),
+            "tiles": tiles,
+            "tile_density_vs_causal_dense": tiles / dense_tiles,
+            "tile_flops": flops,
+            "vs_index_GBps": vs_bytes / (vs_us * 1e-6) / 1e9,
+            "roofline": roofline_prefill,
+        },
+        "roofline": roofline,
+        "kernels": kern,
+        "gpu_launches": int(round(per_step_launches * args.steps)),
+        "e2e": {"value": 1e3 * statistics.mean(e2e), "unit": "us/step",
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "prefill_ms": statistics.mean(pe2e),
+                "prefill_h2d_bytes": int(sum(t.numel() * 2 for t in hp)),
+                "prefill_d2h_bytes": int(h_pout.numel() * 2)},
+        "clocks": clock_info,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

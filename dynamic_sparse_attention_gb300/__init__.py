@@ -14,6 +14,8 @@ from .binding import (  # noqa: F401
     hip_select_workspace_bytes,
     library_path,
     load,
+    profile_collect,
+    profile_enable,
     sparse_attn_decode,
     sparse_attn_decode_workspace_bytes,
     sparse_attn_prefill,

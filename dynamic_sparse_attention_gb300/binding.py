@@ -51,6 +51,10 @@ class VsDebug(ctypes.Structure):
     _fields_ = [("vsum", _vp), ("ssum", _vp)]
 
 
+class KernelStat(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char_p), ("launches", _c_int), ("total_ms", ctypes.c_double)]
+
+
 class DsaError(RuntimeError):
     def __init__(self, fn: str, status: int, msg: str):
         super().__init__(f"{fn} failed with status {status}: {msg}")
@@ -76,7 +80,23 @@ _SIGNATURES = {
                                 ctypes.c_size_t, _vp]),
     "sparse_attn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                      _vp, ctypes.c_float, _vp, _vp, _vp]),
+    "dsa_profile_enable": (_c_int, [_c_int]),
+    "dsa_profile_collect": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_int)]),
 }
+
+
+def profile_enable(on: bool = True) -> None:
+    """Bracket every library kernel launch with CUDA events on its stream."""
+    load().dsa_profile_enable(1 if on else 0)
+
+
+def profile_collect() -> dict:
+    """Wait for the recorded events; {kernel name: (launches, total ms)}, then clear."""
+    lib = load()
+    buf = (KernelStat * 64)()
+    n = _c_int()
+    _check("dsa_profile_collect", lib.dsa_profile_collect(buf, 64, ctypes.byref(n)))
+    return {buf[i].name.decode(): (buf[i].launches, buf[i].total_ms) for i in range(min(n.value, 64))}
 
 
 def library_path() -> str:

@@ -4,9 +4,17 @@
 
 #include "api_common.h"
 #include "launch.h"
+#include "profile.h"
 
 namespace dsa {
 namespace {
+
+const char *const kScoreNames[DSA_MAX_STAGES] = {
+    "hip_stage_score_s0", "hip_stage_score_s1", "hip_stage_score_s2", "hip_stage_score_s3",
+    "hip_stage_score_s4", "hip_stage_score_s5", "hip_stage_score_s6", "hip_stage_score_s7"};
+const char *const kTopkNames[DSA_MAX_STAGES] = {
+    "hip_stage_topk_s0", "hip_stage_topk_s1", "hip_stage_topk_s2", "hip_stage_topk_s3",
+    "hip_stage_topk_s4", "hip_stage_topk_s5", "hip_stage_topk_s6", "hip_stage_topk_s7"};
 
 int check_decode_shape(const dsa_decode_shape *s) {
   if (!s) return fail(DSA_ERR_INVALID_ARG, "shape is NULL");
@@ -157,7 +165,11 @@ int hip_select(const void *q, const void *k, const int32_t *kv_len, const dsa_de
     sa.score = (dbg && dbg->chunk_score[i]) ? dbg->chunk_score[i] : w.score[i];
     sa.dbg_rep = dbg ? dbg->rep[i] : nullptr;
     sa.dbg_rho = dbg ? dbg->rep_score[i] : nullptr;
-    cudaError_t e = launch_stage_score(sa, s);
+    cudaError_t e;
+    {
+      ProfScope ps(kScoreNames[i], s);
+      e = launch_stage_score(sa, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "stage_score launch");
 
     StageTopkArgs ta{};
@@ -179,7 +191,10 @@ int hip_select(const void *q, const void *k, const int32_t *kv_len, const dsa_de
     ta.out_stride = cfg->keep[i];
     ta.dbg_idx = dbg ? dbg->stage_idx[i] : nullptr;
     ta.dbg_cnt = dbg ? dbg->stage_cnt[i] : nullptr;
-    e = launch_stage_topk(ta, s);
+    {
+      ProfScope ps(kTopkNames[i], s);
+      e = launch_stage_topk(ta, s);
+    }
     if (e != cudaSuccess) return cuda_fail(e, "stage_topk launch");
   }
   return DSA_OK;

@@ -1,0 +1,177 @@
+// C-ABI entry points of the prefill half: vs_index_build and sparse_attn_prefill.
+#include <cmath>
+
+#include "api_common.h"
+#include "launch.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kBlock = 64;
+constexpr int kDiagPerTile = 127;
+
+int check_prefill_shape(const dsa_prefill_shape *s) {
+  if (!s) return fail(DSA_ERR_INVALID_ARG, "shape is NULL");
+  if (s->B < 1 || s->B > 65535) return fail(DSA_ERR_INVALID_ARG, "B=%d outside [1, 65535]", s->B);
+  if (s->S < 1) return fail(DSA_ERR_INVALID_ARG, "S=%d < 1", s->S);
+  if (s->H_q < 1 || s->H_kv < 1 || s->H_q % s->H_kv != 0)
+    return fail(DSA_ERR_INVALID_ARG, "H_q=%d must be a positive multiple of H_kv=%d", s->H_q, s->H_kv);
+  if (s->H_q > 65535) return fail(DSA_ERR_INVALID_ARG, "H_q=%d > 65535", s->H_q);
+  if (s->D != 64 && s->D != 128) return fail(DSA_ERR_UNSUPPORTED, "D=%d not in {64, 128}", s->D);
+  return DSA_OK;
+}
+
+int check_vs_cfg(const dsa_prefill_shape *s, const dsa_vs_cfg *c) {
+  if (!c) return fail(DSA_ERR_INVALID_ARG, "cfg is NULL");
+  if (c->block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", c->block);
+  if (c->last_q < 1 || c->last_q > 64)
+    return fail(DSA_ERR_UNSUPPORTED, "last_q=%d outside [1, 64]", c->last_q);
+  if (c->n_vertical < 0 || c->n_vertical > s->S)
+    return fail(DSA_ERR_INVALID_ARG, "n_vertical=%d outside [0, S=%d]", c->n_vertical, s->S);
+  if (c->n_slash < 0 || c->n_slash > s->S)
+    return fail(DSA_ERR_INVALID_ARG, "n_slash=%d outside [0, S=%d]", c->n_slash, s->S);
+  if (s->H_q / s->H_kv > 8)
+    return fail(DSA_ERR_UNSUPPORTED, "H_q/H_kv=%d > 8 query heads per KV head", s->H_q / s->H_kv);
+  const long n_qblk = (s->S + kBlock - 1) / kBlock;
+  const long conv_smem = (2 * ((n_qblk + 31) / 32) + n_qblk + c->n_vertical) * 4;
+  if (conv_smem > 200 * 1024)
+    return fail(DSA_ERR_UNSUPPORTED, "S=%d with n_vertical=%d needs %ld bytes of shared memory",
+                s->S, c->n_vertical, conv_smem);
+  return DSA_OK;
+}
+
+struct VsWs {
+  float *part_m, *part_l, *row_m, *row_l, *vsum, *ssum, *slash_part;
+  size_t bytes;
+  int n_ktile, n_split;
+};
+
+VsWs vs_layout(const dsa_prefill_shape *s, void *base) {
+  VsWs w{};
+  Carve cv(base);
+  const int G = s->H_q / s->H_kv;
+  w.n_ktile = (s->S + kVsKeyTile - 1) / kVsKeyTile;
+  int tps;
+  vs_plan(s->B, s->H_kv, w.n_ktile, &w.n_split, &tps);
+  const size_t rows = static_cast<size_t>(s->B) * s->H_kv * w.n_split * G * 64;
+  w.part_m = cv.take<float>(rows);
+  w.part_l = cv.take<float>(rows);
+  w.row_m = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * 64);
+  w.row_l = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * 64);
+  w.vsum = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * s->S);
+  w.ssum = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * s->S);
+  w.slash_part = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * w.n_ktile * kDiagPerTile);
+  w.bytes = cv.bytes();
+  return w;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int vs_index_build_workspace(const dsa_prefill_shape *shape, const dsa_vs_cfg *cfg, size_t *bytes) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if ((st = check_vs_cfg(shape, cfg))) return st;
+  if (!bytes) return fail(DSA_ERR_ALIGNMENT, "bytes is NULL");
+  *bytes = vs_layout(shape, nullptr).bytes;
+  return DSA_OK;
+}
+
+int vs_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
+                   const dsa_vs_cfg *cfg, int32_t *vertical, int32_t *slash, int32_t *blk_cnt,
+                   int32_t *blk_idx, int32_t *col_cnt, int32_t *col_idx,
+                   const dsa_vs_debug *dbg, void *ws, size_t ws_bytes, void *stream) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if ((st = check_vs_cfg(shape, cfg))) return st;
+  if (!aligned(q, 16) || !aligned(k, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q and k must be non-NULL and 16-byte aligned");
+  if ((cfg->n_vertical > 0 && (!aligned(vertical, 4) || !aligned(col_idx, 4))) ||
+      (cfg->n_slash > 0 && !aligned(slash, 4)) || !aligned(blk_cnt, 4) || !aligned(blk_idx, 4) ||
+      !aligned(col_cnt, 4))
+    return fail(DSA_ERR_ALIGNMENT, "index outputs must be non-NULL and 4-byte aligned");
+  if (dbg && ((dbg->vsum && !aligned(dbg->vsum, 4)) || (dbg->ssum && !aligned(dbg->ssum, 4))))
+    return fail(DSA_ERR_ALIGNMENT, "debug sums must be 4-byte aligned");
+  const VsWs need = vs_layout(shape, nullptr);
+  if (ws_bytes < need.bytes || !aligned(ws, 16))
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu",
+                need.bytes, ws_bytes);
+  const VsWs w = vs_layout(shape, ws);
+  VsArgs a{};
+  a.q = q;
+  a.k = k;
+  a.B = shape->B;
+  a.S = shape->S;
+  a.H_q = shape->H_q;
+  a.H_kv = shape->H_kv;
+  a.D = shape->D;
+  a.last_q = cfg->last_q;
+  a.n_vertical = cfg->n_vertical;
+  a.n_slash = cfg->n_slash;
+  a.scale = 1.0f / std::sqrt(static_cast<float>(shape->D));
+  a.vertical = vertical;
+  a.slash = slash;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  a.col_idx = col_idx;
+  a.row_m = w.row_m;
+  a.row_l = w.row_l;
+  a.part_m = w.part_m;
+  a.part_l = w.part_l;
+  a.vsum = (dbg && dbg->vsum) ? dbg->vsum : w.vsum;
+  a.ssum = (dbg && dbg->ssum) ? dbg->ssum : w.ssum;
+  a.slash_part = w.slash_part;
+  a.n_ktile = w.n_ktile;
+  cudaError_t e = launch_vs_index(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "vs_index_build launch");
+  return DSA_OK;
+}
+
+int sparse_attn_prefill(const void *q, const void *k, const void *v,
+                        const dsa_prefill_shape *shape, int block, int max_blk, int max_col,
+                        const int32_t *blk_cnt, const int32_t *blk_idx, const int32_t *col_cnt,
+                        const int32_t *col_idx, float scale, void *out, float *lse,
+                        void *stream) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
+  if (max_blk < 0 || max_col < 0) return fail(DSA_ERR_INVALID_ARG, "max_blk / max_col negative");
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "scale is not finite");
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q, k, v and out must be non-NULL and 16-byte aligned");
+  if (!aligned(blk_cnt, 4) || !aligned(col_cnt, 4) || (max_blk > 0 && !aligned(blk_idx, 4)) ||
+      (max_col > 0 && !aligned(col_idx, 4)))
+    return fail(DSA_ERR_ALIGNMENT, "list arrays must be non-NULL and 4-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(DSA_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  PrefillArgs a{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.B = shape->B;
+  a.S = shape->S;
+  a.H_q = shape->H_q;
+  a.H_kv = shape->H_kv;
+  a.D = shape->D;
+  a.max_blk = max_blk;
+  a.max_col = max_col;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  a.col_idx = col_idx;
+  a.scale = scale;
+  a.out = out;
+  a.lse = lse;
+  cudaError_t e = launch_prefill_mma(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_prefill launch");
+  return DSA_OK;
+}
+
+}  // extern "C"

@@ -18,6 +18,7 @@
 
 #include "common.cuh"
 #include "launch.h"
+#include "profile.h"
 
 namespace dsa {
 namespace {
@@ -250,10 +251,16 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   dim3 grid(a.n_split, a.H_kv, a.B);
-  kern<<<grid, kNT, smem, s>>>(a);
+  {
+    ProfScope ps("decode_splitk", s);
+    kern<<<grid, kNT, smem, s>>>(a);
+  }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  decode_merge_kernel<T, D><<<a.B * a.T_q * a.H_q, D, 0, s>>>(a);
+  {
+    ProfScope ps("decode_merge", s);
+    decode_merge_kernel<T, D><<<a.B * a.T_q * a.H_q, D, 0, s>>>(a);
+  }
   return cudaGetLastError();
 }
 

@@ -73,14 +73,16 @@ struct VsArgs {
   int32_t *vertical, *slash, *blk_cnt, *blk_idx, *col_cnt, *col_idx;
   float *dbg_vsum, *dbg_ssum;
   // scratch
-  float *row_m, *row_l;       // [B, H_q, last_q] final row max / sum (base-2 logits)
-  float *part_m, *part_l;     // [B, H_kv, n_ktile, G*last_q] per key-tile stats
-  float *vsum, *ssum;         // [B, H_q, S]
-  float *slash_part;          // [B, H_q, n_ktile, KT + last_q - 1]
+  float *row_m, *row_l;       // [B, H_q, 64] final row max / sum (base-2 logits)
+  float *part_m, *part_l;     // [B, H_kv, n_split, G*64] per key-split row stats
+  float *vsum, *ssum;         // [B, H_q, S] column sums / diagonal sums
+  float *slash_part;          // [B, H_q, n_ktile, 127] per key-tile diagonal sums
   int n_ktile;
 };
 cudaError_t launch_vs_index(const VsArgs &a, cudaStream_t s);
 constexpr int kVsKeyTile = 64;
+// number of key splits of the estimate passes (shared by workspace query and launch)
+void vs_plan(int B, int H_kv, int n_ktile, int *n_split, int *tiles_per_split);
 
 // Sparse prefill attention over tile / column lists.
 struct PrefillArgs {
@@ -92,6 +94,6 @@ struct PrefillArgs {
   void *out;
   float *lse;
 };
-cudaError_t launch_prefill(const PrefillArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_mma(const PrefillArgs &a, cudaStream_t s);
 
 }  // namespace dsa

@@ -25,6 +25,7 @@
 #include "common.cuh"
 #include "launch.h"
 #include "mma_sync.cuh"
+#include "profile.h"
 
 namespace dsa {
 namespace {
@@ -38,11 +39,11 @@ template <int D>
 struct VsSmem {
   static constexpr int kRowK = D + 8;  // bf16 elements per padded K row (16-byte pad)
   static constexpr int kPRow = kKT + 4;  // floats per padded P row
-  static size_t bytes(int G, bool pass1) {
+  static size_t bytes(bool pass1) {
     size_t o = 2ull * kKT * kRowK * 2;                             // double-buffered K tiles
     if (pass1) {
-      o += static_cast<size_t>(G) * kRowsPerHead * kPRow * 4;     // P tile per head
-      o += static_cast<size_t>(2 * G) * kKT * 4;                  // per-warp column partials
+      o += static_cast<size_t>(4) * kRowsPerHead * kPRow * 4;     // P tile per head slot
+      o += static_cast<size_t>(8) * kKT * 4;                      // per-warp column partials
     }
     return o;
   }
@@ -51,28 +52,33 @@ struct VsSmem {
 struct VsPassArgs {
   VsArgs a;
   int G, r_q, n_split, tiles_per_split;
+  int n_hgroups;   // CTAs per KV head along y: each serves up to kSlots query heads
 };
+constexpr int kSlots = 4;   // query heads per CTA (two warps each)
 
 template <int D, int PASS>
-__global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
+__global__ void __launch_bounds__(64 * kSlots) vs_pass_kernel(VsPassArgs pa) {
   using SM = VsSmem<D>;
   const VsArgs &a = pa.a;
   extern __shared__ __align__(16) unsigned char smem[];
   uint16_t *s_k = reinterpret_cast<uint16_t *>(smem);
   float *s_P = reinterpret_cast<float *>(smem + 2ull * kKT * SM::kRowK * 2);
-  float *s_col = s_P + static_cast<size_t>(pa.G) * kRowsPerHead * SM::kPRow;
+  float *s_col = s_P + static_cast<size_t>(kSlots) * kRowsPerHead * SM::kPRow;
 
-  const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, b = blockIdx.z;
+  const int g = blockIdx.y / pa.n_hgroups;
+  const int hs0 = (blockIdx.y % pa.n_hgroups) * kSlots;   // first head slot of this CTA
+  const int n_slots = min(kSlots, pa.G - hs0);
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int nthreads = blockDim.x;
   const int G = pa.G, S = a.S, r_q = pa.r_q;
-  const int hs = warp >> 1;                 // head slot inside the group
-  const int h = g * G + hs;
+  const int hs = hs0 + (warp >> 1);         // head slot inside the group
+  const bool slot_ok = hs < G;              // warps past the group's last head stay idle
+  const int h = g * G + (slot_ok ? hs : 0);
   const int row0 = (warp & 1) * 32;         // first of this warp's 32 estimate rows
   const int gq = lane >> 2, tq = lane & 3;
   const int t_begin = split * pa.tiles_per_split;
-  const int t_end = min(a.n_ktile, t_begin + pa.tiles_per_split);
-  if (t_begin >= t_end) return;
+  const int t_end = min(a.n_ktile, t_begin + pa.tiles_per_split);   // empty split: neutral partials
 
   const uint16_t *qg = static_cast<const uint16_t *>(a.q);
   const uint16_t *kg = static_cast<const uint16_t *>(a.k) +
@@ -87,7 +93,7 @@ __global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
 #pragma unroll
     for (int half = 0; half < 2; ++half) {
       const int i = row0 + mb * 16 + gq + half * 8;
-      const bool ok = i < r_q;
+      const bool ok = slot_ok && i < r_q;
       const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
           qg + ((static_cast<size_t>(b) * S + (S - r_q + (ok ? i : 0))) * a.H_q + h) * D);
 #pragma unroll
@@ -109,8 +115,8 @@ __global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
         l_run[mb][hf] = 0.f;
       } else {
         const size_t o = (static_cast<size_t>(b) * a.H_q + h) * kRowsPerHead + i;
-        m_run[mb][hf] = a.row_m[o];
-        const float l = a.row_l[o];
+        m_run[mb][hf] = slot_ok ? a.row_m[o] : -INFINITY;
+        const float l = slot_ok ? a.row_l[o] : 0.f;
         l_run[mb][hf] = l > 0.f ? 1.f / l : 0.f;   // PASS 1 keeps the reciprocal
       }
     }
@@ -127,8 +133,10 @@ __global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
     }
   };
 
-  load_tile(t_begin, 0);
-  cp_async_commit();
+  if (t_begin < t_end) {
+    load_tile(t_begin, 0);
+    cp_async_commit();
+  }
   for (int t = t_begin; t < t_end; ++t) {
     const int buf = (t - t_begin) & 1;
     if (t + 1 < t_end) {
@@ -205,7 +213,7 @@ __global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
         }
     } else {
       // probabilities; column partials over this warp's 32 rows; P tile to smem
-      float *P = s_P + static_cast<size_t>(hs) * kRowsPerHead * SM::kPRow;
+      float *P = s_P + static_cast<size_t>(warp >> 1) * kRowsPerHead * SM::kPRow;
 #pragma unroll
       for (int nb = 0; nb < 8; ++nb) {
         float c0 = 0.f, c1 = 0.f;
@@ -233,21 +241,21 @@ __global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
       }
       __syncthreads();
       // vertical sums: the two warps of a head slot, fixed order
-      for (int e = tid; e < G * kKT; e += nthreads) {
+      for (int e = tid; e < n_slots * kKT; e += nthreads) {
         const int slot = e / kKT, col = e - slot * kKT;
         const int j = j0 + col;
         if (j < S)
-          a.vsum[(static_cast<size_t>(b) * a.H_q + g * G + slot) * S + j] =
+          a.vsum[(static_cast<size_t>(b) * a.H_q + g * G + hs0 + slot) * S + j] =
               s_col[(2 * slot) * kKT + col] + s_col[(2 * slot + 1) * kKT + col];
       }
       // diagonal sums of the tile: u = i - jj + 63, i.e. jj = i + 63 - u
-      for (int e = tid; e < G * kDiag; e += nthreads) {
+      for (int e = tid; e < n_slots * kDiag; e += nthreads) {
         const int slot = e / kDiag, u = e - slot * kDiag;
         const float *Ps = s_P + static_cast<size_t>(slot) * kRowsPerHead * SM::kPRow;
         const int i_lo = max(0, u - (kKT - 1)), i_hi = min(kRowsPerHead - 1, u);
         float s = 0.f;
         for (int i = i_lo; i <= i_hi; ++i) s += Ps[i * SM::kPRow + i + (kKT - 1) - u];
-        a.slash_part[((static_cast<size_t>(b) * a.H_q + g * G + slot) * a.n_ktile + t) * kDiag + u] = s;
+        a.slash_part[((static_cast<size_t>(b) * a.H_q + g * G + hs0 + slot) * a.n_ktile + t) * kDiag + u] = s;
       }
     }
     __syncthreads();
@@ -261,7 +269,7 @@ __global__ void __launch_bounds__(512) vs_pass_kernel(VsPassArgs pa) {
         float l = l_run[mb][hf];
         l += __shfl_xor_sync(kFull, l, 1);
         l += __shfl_xor_sync(kFull, l, 2);
-        if (tq == 0) {
+        if (tq == 0 && slot_ok) {
           const int i = row0 + mb * 16 + gq + hf * 8;
           const size_t o = ((static_cast<size_t>(b) * a.H_kv + g) * pa.n_split + split) *
                                (G * kRowsPerHead) + hs * kRowsPerHead + i;
@@ -443,41 +451,44 @@ cudaError_t launch_vs_d(const VsArgs &a, cudaStream_t s) {
   pa.a = a;
   pa.G = G;
   pa.r_q = r_q;
-  int target = (304 + a.B * a.H_kv - 1) / (a.B * a.H_kv);
-  if (target > a.n_ktile) target = a.n_ktile;
-  pa.tiles_per_split = (a.n_ktile + target - 1) / target;
-  pa.n_split = (a.n_ktile + pa.tiles_per_split - 1) / pa.tiles_per_split;
-  const int threads = 64 * G;   // two warps per head slot
-  dim3 grid(pa.n_split, a.H_kv, a.B);
+  vs_plan(a.B, a.H_kv, a.n_ktile, &pa.n_split, &pa.tiles_per_split);
+  pa.n_hgroups = (G + kSlots - 1) / kSlots;
+  const int threads = 64 * min(G, kSlots);   // two warps per head slot
+  dim3 grid(pa.n_split, a.H_kv * pa.n_hgroups, a.B);
   cudaError_t e;
   {
-    const size_t smem = VsSmem<D>::bytes(G, false);
+    const size_t smem = VsSmem<D>::bytes(false);
     auto k0 = vs_pass_kernel<D, 0>;
     e = cudaFuncSetAttribute(k0, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    ProfScope ps("vs_pass_rowstats", s);
     k0<<<grid, threads, smem, s>>>(pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
     const int total = a.B * a.H_q * kRowsPerHead;
+    ProfScope ps("vs_combine_rowstats", s);
     vs_stats_kernel<<<(total + 255) / 256, 256, 0, s>>>(a, G, pa.n_split);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
-    const size_t smem = VsSmem<D>::bytes(G, true);
+    const size_t smem = VsSmem<D>::bytes(true);
     auto k1 = vs_pass_kernel<D, 1>;
     e = cudaFuncSetAttribute(k1, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    ProfScope ps("vs_pass_sums", s);
     k1<<<grid, threads, smem, s>>>(pa);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
     dim3 g2((a.S + 255) / 256, a.H_q, a.B);
+    ProfScope ps("vs_combine_slash", s);
     vs_slash_kernel<<<g2, 256, 0, s>>>(a, r_q);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   {
     dim3 g3(a.B * a.H_q, 2);
+    ProfScope ps("vs_topk", s);
     vs_topk_kernel<<<g3, kTopkNT, 0, s>>>(a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -488,6 +499,7 @@ cudaError_t launch_vs_d(const VsArgs &a, cudaStream_t s) {
     e = cudaFuncSetAttribute(vs_convert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     dim3 g4((n_qblk + kConvRun - 1) / kConvRun, a.H_q, a.B);
+    ProfScope ps("vs_convert", s);
     vs_convert_kernel<<<g4, kConvNT, smem, s>>>(a, n_qblk);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -496,11 +508,13 @@ cudaError_t launch_vs_d(const VsArgs &a, cudaStream_t s) {
 
 }  // namespace
 
-void vs_plan(int B, int H_kv, int n_ktile, int *n_split) {
+void vs_plan(int B, int H_kv, int n_ktile, int *n_split, int *tiles_per_split) {
+  // about two CTAs per SM of a 152-SM part; every split gets at least one tile
   int target = (304 + B * H_kv - 1) / (B * H_kv);
   if (target > n_ktile) target = n_ktile;
   if (target < 1) target = 1;
   const int tps = (n_ktile + target - 1) / target;
+  *tiles_per_split = tps;
   *n_split = (n_ktile + tps - 1) / tps;
 }
 

@@ -205,6 +205,24 @@ int sparse_attn_prefill(const void *q, const void *k, const void *v,
                         const int32_t *col_idx, float scale, void *out, float *lse,
                         void *stream);
 
+/* ------------------------------------------------------------------ timing */
+
+/* Per-kernel launch timing, off by default.  While enabled, every kernel the
+ * library launches is bracketed by two CUDA events recorded on the call's own
+ * stream (host-side bookkeeping only; nothing changes in the kernels).
+ * dsa_profile_collect waits for the recorded events, returns one entry per
+ * kernel name in first-launch order (name is a static string of the library),
+ * writes min(n, max_out) entries and the total count to *n_out, and clears the
+ * records.  Not a source-page operation: a measurement aid. */
+typedef struct {
+  const char *name;
+  int launches;
+  double total_ms;
+} dsa_kernel_stat;
+
+int dsa_profile_enable(int on);
+int dsa_profile_collect(dsa_kernel_stat *out, int max_out, int *n_out);
+
 /* ------------------------------------------------------------------ helpers */
 
 const char *dsa_last_error(void);   /* last validation / launch message of this thread */

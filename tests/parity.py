@@ -161,3 +161,24 @@ def check_hip_row(case, b, dbg, sel_idx, sel_cnt):
 def attention_errors(o_gpu: np.ndarray, o64: np.ndarray):
     d = np.abs(o_gpu.astype(np.float64) - o64)
     return float(d.max()), float(d.mean())
+
+
+def check_topk_list(vals32: np.ndarray, vals64: np.ndarray, k: int, got: np.ndarray, floor=1e-7):
+    """VS top-k: exact against the rule on the GPU's fp32 values, band rule against fp64."""
+    from oracle import vs as ovs
+    want = ovs.topk_ascending(vals32.astype(np.float64), k)
+    assert np.array_equal(got, want), "GPU top-k differs from the rule on its own values"
+    n = len(vals64)
+    if k >= n or k == 0:
+        return 0
+    order = np.lexsort((np.arange(n), -vals64))
+    hi, lo = vals64[order[k - 1]], vals64[order[k]]
+    tol = REL_BAND * max(abs(hi), abs(lo)) + floor
+    kept = np.zeros(n, bool)
+    kept[got] = True
+    if hi - lo > tol:
+        assert np.array_equal(np.sort(order[:k]), got), "top-k differs outside the tie band"
+        return 0
+    assert kept[vals64 > hi + tol].all(), "an entry above the tie band was dropped"
+    assert not kept[vals64 < lo - tol].any(), "an entry below the tie band was kept"
+    return int(np.sum(kept != np.isin(np.arange(n), order[:k])))
