@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     profile_collect,
     profile_enable,
     sparse_attn_decode,
+    sparse_attn_decode_noalloc,
     sparse_attn_decode_workspace_bytes,
     sparse_attn_prefill,
     vs_index_build,

@@ -80,6 +80,8 @@ _SIGNATURES = {
                                 ctypes.c_size_t, _vp]),
     "sparse_attn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                      _vp, ctypes.c_float, _vp, _vp, _vp]),
+    "sparse_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
+                                            ctypes.c_float, _vp, _vp, _vp, _vp]),
     "dsa_profile_enable": (_c_int, [_c_int]),
     "dsa_profile_collect": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_int)]),
 }
@@ -284,6 +286,33 @@ def sparse_attn_decode(q, k, v, kv_len, sel_idx, sel_cnt, *, n_sink: int, n_stre
                                 ctypes.byref(shape), _ptr(out), _ptr(lse), _ptr(ws),
                                 ctypes.c_size_t(ws.numel()), _stream(stream))
     _check("sparse_attn_decode", st)
+    return out, lse
+
+
+def sparse_attn_decode_noalloc(q, k, v, kv_len, sel_idx, sel_cnt, *, n_sink: int, n_stream: int,
+                               scale: float | None = None, out=None, lse=None,
+                               want_lse: bool = True, stream=None):
+    """sparse_attn_decode whose split-K scratch is the library's built-in device array.
+
+    For callers that must not allocate device memory when they call: nothing is
+    allocated here either when `out` (and `lse`, or want_lse=False) are given.
+    Calls that overlap on the GPU share the one array and must be serialised.
+    """
+    lib = load()
+    _need_cuda(q, k, v, kv_len, sel_idx, sel_cnt)
+    shape = decode_shape(q, k)
+    max_sel = sel_idx.shape[1] if sel_idx is not None else 0
+    if scale is None:
+        scale = shape.D ** -0.5
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None and want_lse:
+        lse = torch.empty(shape.B, shape.T_q, shape.H_q, dtype=torch.float32, device=q.device)
+    st = lib.sparse_attn_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(kv_len), _ptr(sel_idx),
+                                        _ptr(sel_cnt), max_sel, n_sink, n_stream,
+                                        ctypes.c_float(scale), ctypes.byref(shape), _ptr(out),
+                                        _ptr(lse), _stream(stream))
+    _check("sparse_attn_decode_noalloc", st)
     return out, lse
 
 

@@ -142,6 +142,26 @@ int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_
                        int n_stream, float scale, const dsa_decode_shape *shape, void *out,
                        float *lse, void *ws, size_t ws_bytes, void *stream);
 
+/* sparse_attn_decode_noalloc -- the same computation and arguments as
+ * sparse_attn_decode, for callers that cannot allocate device memory when they
+ * call it: a C runtime or plug-in with no device allocator of its own, or a
+ * latency-bound loop that must not call cudaMalloc (which can synchronise the
+ * device).  The pages have no counterpart; this is a packaging variant.
+ * The split-K scratch is a fixed 4 MiB device array inside the library (held
+ * on every GPU that loads the library until the process exits), so no `ws`
+ * argument.  A call whose scratch (sparse_attn_decode_workspace) exceeds
+ * 4 MiB is rejected with DSA_ERR_WORKSPACE and launches nothing.
+ * The first call on a device looks up the array's device address (device
+ * current at the call) and caches it; make that first call before any stream
+ * capture.  All calls share the one array and nothing in it needs clearing
+ * (each call overwrites the slots it reads), but calls that overlap on the
+ * GPU (other streams, other threads) race on it: serialise them. */
+int sparse_attn_decode_noalloc(const void *q, const void *k, const void *v,
+                               const int32_t *kv_len, const int32_t *sel_idx,
+                               const int32_t *sel_cnt, int max_sel, int n_sink, int n_stream,
+                               float scale, const dsa_decode_shape *shape, void *out, float *lse,
+                               void *stream);
+
 /* ------------------------------------------------------------------ prefill */
 
 /* Shape of one causal prefill: q/out [B, S, H_q, D], k/v [B, S, H_kv, D], bf16,
