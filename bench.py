@@ -559,9 +559,11 @@ def main():
             "tile_density_vs_causal_dense": tiles / dense_tiles,
             "tile_flops": flops,
             "vs_index_GBps": vs_bytes / (vs_us * 1e-6) / 1e9,
-            "roofline": roofline_prefill,
         },
-        "roofline": roofline,
+        # the step's dominant kernel (prefill attention, >99% of a step's GPU time)
+        "roofline": roofline_prefill,
+        # the decode half's dominant kernel (the headline `value` is decode us/step)
+        "roofline_decode": roofline,
         "kernels": kern,
         "gpu_launches": int(round(per_step_launches * args.steps)),
         "e2e": {"value": 1e3 * statistics.mean(e2e), "unit": "us/step",
