@@ -8,6 +8,7 @@ has not been built (``__graft_entry__.build()``).
 """
 from .binding import (  # noqa: F401
     DsaError,
+    device_error,
     HipConfig,
     hip_max_chunks,
     hip_select,

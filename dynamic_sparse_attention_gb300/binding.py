@@ -82,9 +82,18 @@ _SIGNATURES = {
                                      _vp, ctypes.c_float, _vp, _vp, _vp]),
     "sparse_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                             ctypes.c_float, _vp, _vp, _vp, _vp]),
+    "dsa_device_error": (_c_int, [ctypes.POINTER(_c_int)]),
     "dsa_profile_enable": (_c_int, [_c_int]),
     "dsa_profile_collect": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_int)]),
 }
+
+
+def device_error() -> int:
+    """Read and clear the library's device error word (0 = no kernel gave up a wait)."""
+    lib = load()
+    c = _c_int()
+    _check("dsa_device_error", lib.dsa_device_error(ctypes.byref(c)))
+    return c.value
 
 
 def profile_enable(on: bool = True) -> None:

@@ -1,5 +1,7 @@
 // C-ABI entry points of the prefill half: vs_index_build and sparse_attn_prefill.
 #include <cmath>
+#include <cstdlib>
+#include <cstring>
 
 #include "api_common.h"
 #include "launch.h"
@@ -169,7 +171,12 @@ int sparse_attn_prefill(const void *q, const void *k, const void *v,
   a.scale = scale;
   a.out = out;
   a.lse = lse;
-  cudaError_t e = launch_prefill_mma(a, static_cast<cudaStream_t>(stream));
+  // tcgen05 kernel by default; DSA_PREFILL_IMPL=mma selects the warp-MMA kernel (used to
+  // compare the two on the same inputs)
+  const char *impl = std::getenv("DSA_PREFILL_IMPL");
+  const bool use_mma = (impl && std::strcmp(impl, "mma") == 0) || !prefill_tc_supported(a);
+  cudaError_t e = use_mma ? launch_prefill_mma(a, static_cast<cudaStream_t>(stream))
+                          : launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_prefill launch");
   return DSA_OK;
 }

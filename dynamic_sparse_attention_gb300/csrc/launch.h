@@ -95,5 +95,8 @@ struct PrefillArgs {
   float *lse;
 };
 cudaError_t launch_prefill_mma(const PrefillArgs &a, cudaStream_t s);
+// tcgen05 version (D in {64, 128}; shared-memory budget bounds S)
+bool prefill_tc_supported(const PrefillArgs &a);
+cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 
 }  // namespace dsa

@@ -243,6 +243,15 @@ typedef struct {
 int dsa_profile_enable(int on);
 int dsa_profile_collect(dsa_kernel_stat *out, int max_out, int *n_out);
 
+/* ------------------------------------------------------------------ diagnostics */
+
+/* Every wait inside the tensor-core prefill is bounded; a CTA that gives up stops
+ * issuing work, frees its resources, writes zero output and sets a device error
+ * word.  dsa_device_error copies that word to *code (0 = none) and clears it.  It
+ * synchronises with the device (cudaMemcpyFromSymbol); call it between steps, not on
+ * a hot path.  Not a source-page operation. */
+int dsa_device_error(int *code);
+
 /* ------------------------------------------------------------------ helpers */
 
 const char *dsa_last_error(void);   /* last validation / launch message of this thread */

@@ -1,5 +1,6 @@
 """GPU parity of the prefill half (vs_index_build + sparse_attn_prefill) against the fp64 oracle."""
 import math
+import os
 
 import numpy as np
 import pytest
@@ -26,6 +27,26 @@ def _lib():
 
 def _dev(c):
     return to_dev(c.q, "bf16"), to_dev(c.k, "bf16"), to_dev(c.v, "bf16")
+
+
+def _with_impl(impl, fn):
+    """Run fn with the prefill kernel forced to `impl` ("mma" or the default tensor-core one)."""
+    old = os.environ.get("DSA_PREFILL_IMPL")
+    os.environ["DSA_PREFILL_IMPL"] = impl
+    try:
+        return fn()
+    finally:
+        if old is None:
+            del os.environ["DSA_PREFILL_IMPL"]
+        else:
+            os.environ["DSA_PREFILL_IMPL"] = old
+
+
+@pytest.fixture(autouse=True)
+def _no_device_errors():
+    yield
+    torch.cuda.synchronize()
+    assert dsa.device_error() == 0, "a prefill CTA gave up a bounded wait"
 
 
 def _check_index(c, idx, heads=None, blocks=None):
@@ -182,3 +203,22 @@ def test_prefill_128k_config():
     for h in (0, 13, 31):
         assert np.isin(c.planted_columns, vert[h]).mean() >= 0.9
         assert np.isin(c.planted_offsets, sl[h]).mean() >= 0.85
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_tensor_core_and_warp_mma_kernels_agree(D):
+    """Both prefill kernels on identical inputs (VS lists and arbitrary lists)."""
+    c = prefill_case("agree", S=1500, H_q=4, H_kv=2, D=D, seed=70 + D, n_vertical=50,
+                     n_slash=300)
+    q, k, v = _dev(c)
+    idx = dsa.vs_index_build(q, k, last_q=c.last_q, n_vertical=c.n_vertical, n_slash=c.n_slash)
+    rand = _random_lists(np.random.default_rng(D), c.S, c.H_q, max_blk=24, max_col=130)
+    for lists in ((idx["blk_cnt"], idx["blk_idx"], idx["col_cnt"], idx["col_idx"]), rand):
+        o_tc, l_tc = dsa.sparse_attn_prefill(q, k, v, *lists)
+        o_mm, l_mm = _with_impl("mma", lambda: dsa.sparse_attn_prefill(q, k, v, *lists))
+        torch.cuda.synchronize()
+        d = (o_tc.float() - o_mm.float()).abs()
+        assert d.max().item() <= MAX_ABS and d.mean().item() <= MEAN_ABS
+        fin = torch.isfinite(l_mm)
+        assert torch.equal(fin, torch.isfinite(l_tc))
+        assert (l_tc[fin] - l_mm[fin]).abs().max().item() <= 1e-3
