@@ -9,7 +9,7 @@
 #include <cstdarg>
 #include <cstdio>
 
-#include "../../include/dsa.h"
+#include "dsa.h"
 
 namespace dsa {
 

@@ -7,20 +7,31 @@
 // mask constant taken as exact exclusion.
 //
 // One CTA computes 128 query rows: the two consecutive 64-row query blocks m0 = 2p and
-// m1 = 2p + 1 of one head, so every MMA has M = 128.  The CTA walks the union of the two
-// blocks' tile lists (ascending key block), then block m0's column tiles, then block
-// m1's; a tile listed for only one of the blocks is masked for the other half's rows.
-// Warp roles (192 threads):
-//   warp 0    producer: Q once (TMA), then per tile K and V (TMA for 64-key blocks,
-//             16-byte cp.async gathers for column tiles) into a 4-stage ring;
-//   warp 1    MMA issuer (one thread): S = Q K^T into a double-buffered TMEM tile
-//             (128 lanes x 64 fp32 columns), O += P V into TMEM (128 x D fp32);
-//   warps 2-5 softmax, one thread per query row: read S from TMEM, mask, online
-//             softmax with the exact running max (when a row's max grows, O in TMEM
-//             is rescaled once the previous P V has retired, so the largest
-//             probability of a row is exactly 1 and carries no bf16 rounding), write
-//             P (bf16) to shared memory in the 128-byte-swizzled K-major layout the
-//             MMA reads, and at the end normalise O and store it.
+// m1 = 2p + 1 of one head.  Keys go through the tensor core in 128-key tiles (two
+// consecutive 64-key list blocks): at M = N = K = 128 the MMA runs at its full rate,
+// while 64-key tiles (Q K^T with N = 64, P V with K = 64) reach well under half of it.
+// The CTA walks the 128-key tiles that hold a listed block of either query block
+// (descending, so the running max settles early), then block m0's gathered column tiles
+// (128 columns each), then block m1's; a row masks the 64-key halves its own query
+// block does not list, keys after it (causal) and keys past the sequence end.
+// Warp roles (352 threads):
+//   warp 0     K producer: Q once (TMA), then K tiles (TMA for block tiles, 16-byte
+//              cp.async gathers for column tiles) into a 3-stage ring; writes each
+//              tile's description (kind, key tile, per-half membership, positions);
+//   warp 1     V producer: V tiles into a 2-stage ring (its own walk of the same list);
+//   warp 2     MMA issuer (one thread): S_x = Q K^T (M = N = 128, K = D) into TMEM, then
+//              O_x += P V (A = P read from TMEM, 128 keys), x = tile parity;
+//   warps 3-10 softmax: two independent warpgroups; warpgroup x owns the tiles of
+//              parity x (S_x, O_x, its running max and row sum), one thread per query
+//              row (warp w reads the TMEM lanes of quarter w % 4).  Pass 1 takes the
+//              masked row max; pass 2 forms P = exp2(s * scale * log2e - max) with the
+//              exact running max of the stream (its largest probability is exactly 1,
+//              free of bf16 rounding) and writes P as bf16 pairs over the first 64
+//              columns of S_x, where the P V MMA reads it.  O_x is brought to the
+//              stream's current max before P is released (the stream's previous P V
+//              retired before the Q K^T that filled S_x, as one thread issues both in
+//              order).  The epilogue merges the two streams (log-sum-exp), normalises
+//              and stores.
 // Operands: Q and K tiles are K-major with 128-byte swizzle (what TMA writes for a
 // 64-element-wide box); V tiles are the B operand in MN-major form (keys along K).
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work, drains its
@@ -31,6 +42,7 @@
 
 #include <atomic>
 #include <cstdlib>
+#include <cstddef>
 #include <cstring>
 #include <mutex>
 
@@ -46,11 +58,14 @@ namespace {
 
 using namespace tc;
 
-constexpr int kRowsQ = 128;       // query rows per CTA
-constexpr int kKeys = 64;         // keys per tile
-constexpr int kNS = 4;            // K/V pipeline stages
-constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr int kRowsQ = 128;        // query rows per CTA
+constexpr int kBlk = 64;           // block size of the tile lists
+constexpr int kKeys = 128;         // keys per MMA tile (two list blocks)
+constexpr int kKS = 3;             // K ring stages
+constexpr int kVS = 2;             // V ring stages
+constexpr int kMetaRing = 8;       // tile descriptions in flight (the K ring runs at most 6 ahead)
+constexpr int kThreads = 11 * 32;  // K producer, V producer, MMA issuer, 8 softmax warps
+constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -59,29 +74,34 @@ static __device__ int g_abort_epoch;         // launch epoch of a launch in whic
 constexpr uint64_t kWaitLimitNs = 500000000ull;
 
 struct TileMeta {
-  int kind;          // 0: 64-key block, 1: gathered column tile
-  int n;             // key block (kind 0)
-  int mask;          // bit 0: rows of block m0 use the tile, bit 1: rows of block m1
+  int kind;          // 0: 128-key block tile, 1: gathered column tile
+  int n;             // 128-key tile index (kind 0)
+  int mask;          // bit 2*grp + half: rows of query block m_grp use that 64-key half
   int ncols;
   int pos[kKeys];    // key positions of a column tile (-1: empty slot)
 };
+static_assert(sizeof(TileMeta) % 16 == 0 && offsetof(TileMeta, pos) % 16 == 0, "int4 reads of pos");
 
 template <int D>
 struct Layout {
   static constexpr int kHalves = D / 64;
-  static constexpr uint32_t kQHalf = kRowsQ * 128;          // 128 rows x 128 bytes
-  static constexpr uint32_t kKVHalf = kKeys * 128;          // 64 rows x 128 bytes
-  static constexpr uint32_t kStage = 2 * kHalves * kKVHalf;   // K halves, then V halves
-  static constexpr uint32_t kP = kRowsQ * 128;              // 128 rows x 64 bf16
+  static constexpr uint32_t kQHalf = kRowsQ * 128;          // 128 rows x 64 dims
+  static constexpr uint32_t kHalf = kKeys * 128;            // 128 keys x 64 dims
+  static constexpr uint32_t kTile = kHalves * kHalf;        // one K or V tile
   static constexpr uint32_t oQ = 0;
-  static constexpr uint32_t oStage = oQ + kHalves * kQHalf;
-  static constexpr uint32_t oP = oStage + kNS * kStage;
-  static constexpr uint32_t oMeta = oP + 2 * kP;
-  static constexpr uint32_t oBar = oMeta + kNS * sizeof(TileMeta);
-  static constexpr int kBars = 2 * kNS + 8;
+  static constexpr uint32_t oK = oQ + kHalves * kQHalf;
+  static constexpr uint32_t oV = oK + kKS * kTile;
+  static constexpr uint32_t oMeta = oV + kVS * kTile;
+  static constexpr uint32_t oBar = oMeta + kMetaRing * sizeof(TileMeta);
+  static constexpr int kBars = 2 * kKS + 2 * kVS + 9;
   static constexpr uint32_t oMisc = oBar + kBars * 8;
-  static constexpr uint32_t oBits = oMisc + 64;
+  static constexpr uint32_t oXch = oMisc + 64;              // [2 streams][128 rows] x (max, sum)
+  static constexpr uint32_t oBits = oXch + 2048;
   static size_t bytes(int n_words) { return oBits + 8ull * n_words + 1024; }
+  // TMEM columns (32-bit): S_0, S_1 (P_x over the first 64 columns of S_x) | O_0, O_1
+  static constexpr uint32_t cO = 2 * kKeys;
+  static_assert(cO + 2 * D <= kTmemCols, "TMEM columns");
+  static_assert(oQ % 1024 == 0 && oK % 1024 == 0 && oV % 1024 == 0, "swizzle atoms");
 };
 
 struct TcArgs {
@@ -107,9 +127,9 @@ __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, const Wa
   const uint64_t t0 = global_ns();
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
     if (*w.cta_abort) return false;
-    if ((++spins & 31u) == 0u) {
+    if ((++spins & 7u) == 0u) {
       if (*reinterpret_cast<volatile int *>(&g_abort_epoch) == w.epoch) {
         *w.cta_abort = 1;
         return false;
@@ -139,15 +159,50 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return ok != 0;
 }
 
+// even bit 2i set <=> block 2i or 2i+1 of the word is listed
+__device__ __forceinline__ uint32_t pair_bits(uint32_t u) { return (u | (u >> 1)) & 0x55555555u; }
+
+// Walk over the 128-key tiles that hold a listed 64-key block of either query block,
+// in descending key order (run by one lane).  Scores near the diagonal are usually the
+// largest of a row, so visiting them first settles the running max early and spares
+// most rescalings of the accumulator.
+struct TileWalk {
+  const uint32_t *bm0, *bm1;
+  int wi;
+  uint32_t cur;
+  __device__ void init(const uint32_t *b0, const uint32_t *b1, int nw) {
+    bm0 = b0;
+    bm1 = b1;
+    wi = nw - 1;
+    cur = nw > 0 ? pair_bits(bm0[wi] | bm1[wi]) : 0u;
+  }
+  // next tile and its membership mask; false once the bitmaps run out
+  __device__ bool next(int &tile, int &mask) {
+    while (cur == 0u && wi > 0) {
+      --wi;
+      cur = pair_bits(bm0[wi] | bm1[wi]);
+    }
+    if (cur == 0u) return false;
+    const int bit = 31 - __clz(cur);
+    cur &= ~(1u << bit);
+    tile = (wi * 32 + bit) >> 1;
+    const uint32_t w0 = bm0[wi] >> bit, w1 = bm1[wi] >> bit;
+    mask = static_cast<int>((w0 & 1u) | (((w0 >> 1) & 1u) << 1) | ((w1 & 1u) << 2) |
+                            (((w1 >> 1) & 1u) << 3));
+    return true;
+  }
+};
+
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcArgs a) {
   using L = Layout<D>;
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
-  uint64_t *kv_full = bars, *kv_empty = bars + kNS;
-  uint64_t *s_full = bars + 2 * kNS, *p_full = s_full + 2, *pv_done = p_full + 2;
-  uint64_t *q_full = pv_done + 2, *fin = q_full + 1;
+  uint64_t *k_full = bars, *k_empty = k_full + kKS;
+  uint64_t *v_full = k_empty + kKS, *v_empty = v_full + kVS;
+  uint64_t *s_full = v_empty + kVS, *p_full = s_full + 2, *pv_done = p_full + 2;
+  uint64_t *q_full = pv_done + 2, *fin = q_full + 1, *xfin = fin + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::oMisc + 4);
   int *n_blk_tiles_s = reinterpret_cast<int *>(sm + L::oMisc + 8);
@@ -158,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int n_pairs = (a.n_qblk + 1) / 2;
-  const int p = n_pairs - 1 - static_cast<int>(blockIdx.x);
+  const int p = n_pairs - 1 - static_cast<int>(blockIdx.x);   // longest rows first
   const int h = blockIdx.y, b = blockIdx.z;
   const int g = h / (a.H_q / a.H_kv);
   const int m0 = 2 * p, m1 = 2 * p + 1;
@@ -166,20 +221,21 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const size_t bh = static_cast<size_t>(b) * a.H_q + h;
 
   if (tid == 0) {
-    for (int i = 0; i < 2 * kNS; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < 2 * kKS + 2 * kVS; ++i) mbar_init(&bars[i], 1);
     mbar_init(&s_full[0], 1);
     mbar_init(&s_full[1], 1);
-    mbar_init(&p_full[0], 128);
-    mbar_init(&p_full[1], 128);
+    mbar_init(&p_full[0], 4);     // one arrival per softmax warp of the stream
+    mbar_init(&p_full[1], 4);
     mbar_init(&pv_done[0], 1);
     mbar_init(&pv_done[1], 1);
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
+    mbar_init(xfin, 8);           // one arrival per softmax warp
     *abort_flag = 0;
     *n_blk_tiles_s = 0;
     fence_mbar_init();
   }
-  if (warp == 1) {
+  if (warp == 2) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
@@ -205,7 +261,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   {
     int cnt = 0;
-    for (int w = tid; w < a.n_words; w += kThreads) cnt += __popc(bm0[w] | bm1[w]);
+    for (int w = tid; w < a.n_words; w += kThreads) cnt += __popc(pair_bits(bm0[w] | bm1[w]));
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
     if (lane == 0 && cnt) atomicAdd(n_blk_tiles_s, cnt);
@@ -220,115 +276,139 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const int T = n_blk_t + nct0 + nct1;
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp == 0 || warp == 1) {
+    // ------------------------------------------------------------ producers (K: warp 0, V: warp 1)
+    const bool is_k = warp == 0;
+    const int NS = is_k ? kKS : kVS;
+    uint64_t *full = is_k ? k_full : v_full;
+    uint64_t *empty = is_k ? k_empty : v_empty;
+    unsigned char *ring = sm + (is_k ? L::oK : L::oV);
+    const CUtensorMap *map = is_k ? &a.tk : &a.tv;
+    const uint16_t *src = (is_k ? a.k : a.v) + (static_cast<size_t>(b) * a.S * a.H_kv + g) * D;
+    const size_t krow = static_cast<size_t>(a.H_kv) * D;
+    if (is_k && lane == 0) {
       mbar_arrive_expect_tx(q_full, L::kHalves * L::kQHalf);
       for (int hh = 0; hh < L::kHalves; ++hh)
         tma_load_4d(sm + L::oQ + hh * L::kQHalf, &a.tq, q_full, 64 * hh, h, kRowsQ * p, b);
     }
-    int wi = 0;
-    uint32_t cur = a.n_words > 0 ? (bm0[0] | bm1[0]) : 0u;
+    TileWalk walk;
+    walk.init(bm0, bm1, a.n_words);
     int issued = 0;
-    const size_t krow = static_cast<size_t>(a.H_kv) * D;
-    const uint16_t *kb = a.k + (static_cast<size_t>(b) * a.S * a.H_kv + g) * D;
-    const uint16_t *vb = a.v + (static_cast<size_t>(b) * a.S * a.H_kv + g) * D;
     for (int t = 0; t < T; ++t) {
-      const int st = t % kNS;
-      if (t >= kNS && !warp_wait(&kv_empty[st], ((t / kNS) - 1) & 1, wc)) break;
-      unsigned char *stage = sm + L::oStage + st * L::kStage;
-      TileMeta *md = &meta[st];
+      const int st = t % NS;
+      if (t >= NS && !warp_wait(&empty[st], ((t / NS) - 1) & 1, wc)) break;
+      unsigned char *stage = ring + st * L::kTile;
       if (t < n_blk_t) {
-        if (lane == 0 && cur == 0u) {
-          while (cur == 0u && wi + 1 < a.n_words) {
-            ++wi;
-            cur = bm0[wi] | bm1[wi];
-          }
-          if (cur == 0u) *abort_flag = 1;   // count and bitmaps disagree: stop cleanly
-        }
-        if (__shfl_sync(kFull, static_cast<int>(*abort_flag), 0)) break;
+        int tile = 0, mask = 0, ok = 1;
         if (lane == 0) {
-          const int n = wi * 32 + __ffs(cur) - 1;
-          cur &= cur - 1u;
-          md->kind = 0;
-          md->n = n;
-          md->mask = ((bm0[n >> 5] >> (n & 31)) & 1u) | (((bm1[n >> 5] >> (n & 31)) & 1u) << 1);
-          md->ncols = kKeys;
-          mbar_arrive_expect_tx(&kv_full[st], L::kStage);
+          ok = walk.next(tile, mask) ? 1 : 0;
+          if (!ok) *abort_flag = 1;   // count and bitmaps disagree: stop cleanly
+        }
+        if (!__shfl_sync(kFull, ok, 0)) break;
+        if (lane == 0) {
+          if (is_k) {
+            TileMeta *md = &meta[t % kMetaRing];
+            md->kind = 0;
+            md->n = tile;
+            md->mask = mask;
+            md->ncols = kKeys;
+          }
+          mbar_arrive_expect_tx(&full[st], L::kTile);
           for (int hh = 0; hh < L::kHalves; ++hh)
-            tma_load_4d(stage + hh * L::kKVHalf, &a.tk, &kv_full[st], 64 * hh, g, kKeys * n, b);
-          for (int hh = 0; hh < L::kHalves; ++hh)
-            tma_load_4d(stage + (L::kHalves + hh) * L::kKVHalf, &a.tv, &kv_full[st], 64 * hh, g,
-                        kKeys * n, b);
+            tma_load_4d(stage + hh * L::kHalf, map, &full[st], 64 * hh, g, kKeys * tile, b);
         }
       } else {
         const int ct = t - n_blk_t;
         const int grp = ct < nct0 ? 0 : 1;
         const int cb = (grp == 0 ? ct : ct - nct0) * kKeys;
         const int mg = grp == 0 ? m0 : m1;
-        const int cg = grp == 0 ? c0 : c1;
+        const int ncol = min(kKeys, (grp == 0 ? c0 : c1) - cb);
         const int32_t *cl = a.col_idx + (bh * a.n_qblk + mg) * static_cast<size_t>(a.max_col);
-        const int ncol = min(kKeys, cg - cb);
-        const int last_row = min(kKeys * mg + kKeys - 1, a.S - 1);
-        for (int x = lane; x < kKeys; x += 32) {
+        const int last_row = min(kBlk * mg + kBlk - 1, a.S - 1);
+        int pos[kKeys / 32];
+#pragma unroll
+        for (int i = 0; i < kKeys / 32; ++i) {
+          const int x = lane + 32 * i;
           int j = x < ncol ? cl[cb + x] : -1;
           if (j < 0 || j > last_row) j = -1;
-          md->pos[x] = j;
+          pos[i] = j;
         }
-        if (lane == 0) {
-          md->kind = 1;
-          md->n = -1;
-          md->mask = 1 << grp;
-          md->ncols = ncol;
+        if (is_k) {
+          TileMeta *md = &meta[t % kMetaRing];
+#pragma unroll
+          for (int i = 0; i < kKeys / 32; ++i) md->pos[lane + 32 * i] = pos[i];
+          if (lane == 0) {
+            md->kind = 1;
+            md->n = -1;
+            md->mask = grp == 0 ? 0x3 : 0xC;
+            md->ncols = ncol;
+          }
         }
-        __syncwarp();
-        constexpr int CPR = D / 8;   // 16-byte chunks per row
-        for (int e = lane; e < 2 * kKeys * CPR; e += 32) {
-          const int which = e / (kKeys * CPR);
-          const int rem = e - which * (kKeys * CPR);
-          const int x = rem / CPR, c = rem - x * CPR;
+        // key row x = lane + 32 i; 16-byte chunk c lies in dims half c >> 3, swizzled in its row
+#pragma unroll 1
+        for (int c = 0; c < D / 8; ++c) {
           const int hh = c >> 3, cc = c & 7;
-          unsigned char *dst = stage + (which * L::kHalves + hh) * L::kKVHalf + x * 128 +
-                               ((cc ^ (x & 7)) << 4);
-          const int j = md->pos[x];
-          if (j >= 0) cp_async_16(dst, (which ? vb : kb) + static_cast<size_t>(j) * krow + c * 8);
-          else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+#pragma unroll
+          for (int i = 0; i < kKeys / 32; ++i) {
+            const int x = lane + 32 * i;
+            unsigned char *dst = stage + hh * L::kHalf + x * 128 + ((cc ^ (x & 7)) << 4);
+            if (pos[i] >= 0) cp_async_16(dst, src + static_cast<size_t>(pos[i]) * krow + c * 8);
+            else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
+          }
         }
+        cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&kv_full[st]);
+        if (lane == 0) mbar_arrive(&full[st]);
       }
       ++issued;
     }
     if (*abort_flag && lane == 0) {
-      // let this CTA's copies land before it exits
-      for (int t = max(0, issued - kNS); t < issued; ++t)
-        drain_wait(&kv_full[t % kNS], (t / kNS) & 1, 200000000ull);
-      drain_wait(q_full, 0, 200000000ull);
+      // let this CTA's bulk copies land before it exits
+      for (int t = max(0, issued - NS); t < issued; ++t)
+        drain_wait(&full[t % NS], (t / NS) & 1, 200000000ull);
+      if (is_k) drain_wait(q_full, 0, 200000000ull);
     }
-  } else if (warp == 1) {
+  } else if (warp == 2) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
       constexpr uint32_t id_qk = idesc_bf16_f32(kRowsQ, kKeys, false, false);
       constexpr uint32_t id_pv = idesc_bf16_f32(kRowsQ, D, false, true);
       const uint32_t sQ = smem_u32(sm + L::oQ);
-      const uint32_t sS = smem_u32(sm + L::oStage);
-      const uint32_t sP = smem_u32(sm + L::oP);
+      const uint32_t sK = smem_u32(sm + L::oK);
+      const uint32_t sV = smem_u32(sm + L::oV);
       bool ok = tc_wait(q_full, 0, wc);
       auto issue_qk = [&](int t) -> bool {
-        const int st = t % kNS;
-        if (!tc_wait(&kv_full[st], (t / kNS) & 1, wc)) return false;
+        const int st = t % kKS;
+        if (!tc_wait(&k_full[st], (t / kKS) & 1, wc)) return false;
         tc_fence_after();
         const uint32_t d = tmem + static_cast<uint32_t>((t & 1) * kKeys);
-        const uint32_t kbase = sS + st * L::kStage;
+        const uint32_t kbase = sK + st * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint64_t ad = sdesc_sw128(sQ + (kk >> 2) * L::kQHalf + (kk & 3) * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kKVHalf + (kk & 3) * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
           tc_mma(d, ad, bd, id_qk, kk > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[t & 1]);
+        tc_commit(&k_empty[st]);
+        return true;
+      };
+      auto issue_pv = [&](int t) -> bool {
+        const int st = t % kVS;
+        if (!tc_wait(&v_full[st], (t / kVS) & 1, wc)) return false;
+        tc_fence_after();
+        const uint32_t vbase = sV + st * L::kTile;
+        const uint32_t pcol = tmem + static_cast<uint32_t>((t & 1) * kKeys);
+        const uint32_t ocol = tmem + L::cO + static_cast<uint32_t>((t & 1) * D);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk) {
+          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kHalf, 1024);
+          tc_mma_ts(ocol, pcol + kk * 8, bd, id_pv, (t >= 2 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(&pv_done[t & 1]);
+        tc_commit(&v_empty[st]);
         return true;
       };
       if (ok && T > 0) ok = issue_qk(0);
@@ -336,146 +416,188 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (t + 1 < T && !(ok = issue_qk(t + 1))) break;
         if (!(ok = tc_wait(&p_full[t & 1], (t >> 1) & 1, wc))) break;
         tc_fence_after();
-        const uint32_t vbase = sS + (t % kNS) * L::kStage + L::kHalves * L::kKVHalf;
-        const uint32_t pbase = sP + (t & 1) * L::kP;
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk) {
-          const uint64_t ad = sdesc_sw128(pbase + kk * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kKVHalf, 1024);
-          tc_mma(tmem + 2 * kKeys, ad, bd, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
-        }
-        tc_commit(&pv_done[t & 1]);
-        tc_commit(&kv_empty[t % kNS]);
+        ok = issue_pv(t);
       }
       tc_commit(fin);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    const int wg = (warp - 3) >> 2;   // stream: tiles t with t % 2 == wg
     const int quarter = warp & 3;
     const int row = quarter * 32 + lane;
     const int grp = row >> 6;
     const int qpos = kRowsQ * p + row;
     const bool row_ok = qpos < a.S;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    float m_ref = -INFINITY, l = 0.f;
+    const uint32_t s_col = tl + static_cast<uint32_t>(wg * kKeys);   // S_wg (P_wg over its start)
+    const uint32_t o_col = tl + L::cO + static_cast<uint32_t>(wg * D);
+    const float sl2 = a.sl2;
+    const int last_key = min(qpos, a.S - 1);   // causal and in-sequence bound of the row
+    float m_cur = -INFINITY, l = 0.f;   // stream's running max (base-2 units) and row sum
+    float m_o = -INFINITY;              // max that O_wg is currently relative to
     bool ok = true;
-    for (int t = 0; t < T; ++t) {
-      const int sb = t & 1;
-      if (!(ok = warp_wait(&s_full[sb], (t >> 1) & 1, wc))) break;
+    const float2 sl2x2 = make_float2(sl2, sl2);
+    for (int t = wg; t < T; t += 2) {
+      if (!(ok = warp_wait(&s_full[wg], (t >> 1) & 1, wc))) break;
       tc_fence_after();
-      uint32_t sr[2 * 32];
-      tmem_ld32(tl + sb * kKeys, sr);
-      tmem_ld32(tl + sb * kKeys + 32, sr + 32);
-      tmem_wait_ld();
-      const TileMeta *md = &meta[t % kNS];
+      const TileMeta *md = &meta[t % kMetaRing];
       const int kind = md->kind;
-      const bool member = row_ok && ((md->mask >> grp) & 1);
-      float mt = -INFINITY;
-      if (!member) {
+      const int hmask = row_ok ? (md->mask >> (2 * grp)) & 3 : 0;   // halves this row uses
+      const int lim = last_key - kKeys * md->n;   // block tile: slots c <= lim are the row's keys
+      const bool trim = kind != 0 || hmask != 3 || lim < kKeys - 1;   // some slot is not the row's
+      // -inf over the slots [c0, c0 + N) that are not keys of this row
+      auto mask_slots = [&](uint32_t *v, const int c0, const int N) {
+        if (kind == 0) {
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) sr[c] = __float_as_uint(-INFINITY);
-      } else if (kind == 0) {
-        const int lim = min(qpos, a.S - 1) - kKeys * md->n;   // slots 0..lim are keys <= row
-        if (lim >= kKeys - 1) {
-#pragma unroll
-          for (int c = 0; c < kKeys; ++c) {
-            const float x = __uint_as_float(sr[c]) * a.sl2;
-            sr[c] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
-          }
+          for (int c = 0; c < N; ++c)
+            if (!((hmask >> ((c0 + c) >> 6)) & 1) || c0 + c > lim) v[c] = __float_as_uint(-INFINITY);
         } else {
+          const int4 *pp = reinterpret_cast<const int4 *>(md->pos + c0);
 #pragma unroll
-          for (int c = 0; c < kKeys; ++c) {
-            const float x = c <= lim ? __uint_as_float(sr[c]) * a.sl2 : -INFINITY;
-            sr[c] = __float_as_uint(x);
-            mt = fmaxf(mt, x);
+          for (int c4 = 0; c4 < N / 4; ++c4) {
+            const int4 j = pp[c4];
+            if (hmask == 0 || j.x < 0 || j.x > qpos) v[4 * c4] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.y < 0 || j.y > qpos) v[4 * c4 + 1] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.z < 0 || j.z > qpos) v[4 * c4 + 2] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.w < 0 || j.w > qpos) v[4 * c4 + 3] = __float_as_uint(-INFINITY);
           }
         }
-      } else {
+      };
+      // pass 1, 64 keys at a time: masked row max of the tile (four max chains)
+      float mx[4];
 #pragma unroll
-        for (int c = 0; c < kKeys; ++c) {
-          const int j = md->pos[c];
-          const float x = (j >= 0 && j <= qpos) ? __uint_as_float(sr[c]) * a.sl2 : -INFINITY;
-          sr[c] = __float_as_uint(x);
-          mt = fmaxf(mt, x);
-        }
+      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t s[64];
+        tmem_ld32(s_col + 64 * hf, s);
+        tmem_ld32(s_col + 64 * hf + 32, s + 32);
+        tmem_wait_ld();
+        if (trim) mask_slots(s, 64 * hf, 64);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2)
+          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
       }
-      const bool resc = m_ref != -INFINITY && mt > m_ref;
-      if (__any_sync(kFull, resc)) {
-        // O holds PV_{t-1}'s result only after it completes
-        if (t >= 1 && !(ok = warp_wait(&pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, wc))) break;
-        tc_fence_after();
-        const float f = resc ? exp2f(m_ref - mt) : 1.f;
+      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;   // sl2 > 0 keeps the order
+      if (mt > m_cur) {
+        if (m_cur != -INFINITY) l *= fast_exp2(m_cur - mt);
+        m_cur = mt;
+      }
+      // pass 2, 64 keys at a time: probabilities -> bf16 pairs over the first 64 columns
+      // of S_wg (half hf lands on columns 32hf..32hf+31, which pass 2 has already read)
+      const float nm = m_cur == -INFINITY ? 0.f : -m_cur;   // no key yet: every s is -inf
+      const float2 nm2 = make_float2(nm, nm);
+      float2 acc[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t s[64], pk[32];
+        tmem_ld32(s_col + 64 * hf, s);
+        tmem_ld32(s_col + 64 * hf + 32, s + 32);
+        tmem_wait_ld();
+        if (trim) mask_slots(s, 64 * hf, 64);
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) {
+          const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nm2);
+          const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
+          acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+          pk[c >> 1] = pack_bf16x2(e.x, e.y);
+        }
+        tmem_st32(s_col + 32 * hf, pk);
+      }
+      const float2 a01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
+      l += a01.x + a01.y;
+      // O_wg to the current max.  The stream's previous P V has retired: the Q K^T that
+      // filled S_wg was issued after it by the same thread and completes after it.
+      const bool stale = m_o != -INFINITY && m_o < m_cur;
+      if (__any_sync(kFull, stale)) {
+        const float f = stale ? fast_exp2(m_o - m_cur) : 1.f;
+        const float2 f2 = make_float2(f, f);
 #pragma unroll 1
         for (int ch = 0; ch < D / 32; ++ch) {
           uint32_t o[32];
-          tmem_ld32(tl + 2 * kKeys + ch * 32, o);
+          tmem_ld32(o_col + ch * 32, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * f);
-          tmem_st32(tl + 2 * kKeys + ch * 32, o);
-        }
-        tmem_wait_st();
-        if (resc) {
-          l *= f;
-          m_ref = mt;
+          for (int i = 0; i < 32; i += 2) {
+            const float2 y = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2);
+            o[i] = __float_as_uint(y.x);
+            o[i + 1] = __float_as_uint(y.y);
+          }
+          tmem_st32(o_col + ch * 32, o);
         }
       }
-      if (m_ref == -INFINITY) m_ref = mt;
-      uint32_t pk[kKeys / 2];
-      float ps = 0.f;
-#pragma unroll
-      for (int c = 0; c < kKeys; c += 2) {
-        float p0 = 0.f, p1 = 0.f;
-        if (m_ref != -INFINITY) {
-          p0 = fast_exp2(__uint_as_float(sr[c]) - m_ref);
-          p1 = fast_exp2(__uint_as_float(sr[c + 1]) - m_ref);
-        }
-        ps += p0 + p1;
-        pk[c >> 1] = pack_bf16x2(p0, p1);
-      }
-      l += ps;
-      // the P buffer is free once PV_{t-2} has completed
-      if (t >= 2 && !(ok = warp_wait(&pv_done[sb], ((t - 2) >> 1) & 1, wc))) break;
-      unsigned char *prow = sm + L::oP + sb * L::kP + row * 128;
-#pragma unroll
-      for (int c = 0; c < 8; ++c)
-        *reinterpret_cast<uint4 *>(prow + ((c ^ (row & 7)) << 4)) =
-            make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-      fence_proxy_async_smem();
+      m_o = m_cur;
+      tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&p_full[sb]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[wg]);
     }
-    const bool have_o = ok && T > 0 && warp_wait(&pv_done[(T - 1) & 1], ((T - 1) >> 1) & 1, wc);
-    if (have_o) tc_fence_after();
-    const float inv = (have_o && l > 0.f) ? 1.f / l : 0.f;
-    uint16_t *orow = a.out + ((static_cast<size_t>(b) * a.S + (row_ok ? qpos : 0)) * a.H_q + h) * D;
+    // this stream's last P V, if it has tiles
+    const bool mine = T > wg;
+    const int t_last = mine ? wg + 2 * ((T - 1 - wg) >> 1) : 0;
+    if (ok && mine) ok = warp_wait(&pv_done[wg], (t_last >> 1) & 1, wc);
+    // publish (max, sum) of this stream; read the other one
+    float *xch = reinterpret_cast<float *>(sm + L::oXch);
+    xch[(wg * kRowsQ + row) * 2] = (ok && mine) ? m_cur : -INFINITY;
+    xch[(wg * kRowsQ + row) * 2 + 1] = (ok && mine) ? l : 0.f;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(xfin);
+    const bool have_x = warp_wait(xfin, 0, wc);
+    tc_fence_after();
+    const float ma = xch[row * 2], la = xch[row * 2 + 1];
+    const float mb = xch[(kRowsQ + row) * 2], lb = xch[(kRowsQ + row) * 2 + 1];
+    const float m = fmaxf(ma, mb);
+    const float wa = (ma != -INFINITY) ? exp2f(ma - m) : 0.f;
+    const float wb = (mb != -INFINITY) ? exp2f(mb - m) : 0.f;
+    const float lt = la * wa + lb * wb;
+    // both streams' accumulators are final once every softmax warp has published
+    const bool ld_ok = have_x && ok;   // warp-uniform: the TMEM loads are collective
+    const bool good = ld_ok && lt > 0.f;
+    const float inv = good ? 1.f / lt : 0.f;
+    const float fa = wa * inv, fb = wb * inv;
+    const bool use_a = T > 0, use_b = T > 1;
+    // stream wg writes columns [wg * D/2, (wg + 1) * D/2) of the output row
+    uint16_t *orow = a.out + ((static_cast<size_t>(b) * a.S + (row_ok ? qpos : 0)) * a.H_q + h) * D +
+                     wg * (D / 2);
 #pragma unroll 1
-    for (int ch = 0; ch < D / 32; ++ch) {
-      uint32_t o[32];
-      if (have_o) {
-        tmem_ld32(tl + 2 * kKeys + ch * 32, o);
-        tmem_wait_ld();
-      }
+    for (int ch = 0; ch < D / 64; ++ch) {
+      uint32_t oa[32], ob[32];
+      const uint32_t col = static_cast<uint32_t>(wg * (D / 2) + ch * 32);
+      if (ld_ok && use_a) tmem_ld32(tl + L::cO + col, oa);
+      if (ld_ok && use_b) tmem_ld32(tl + L::cO + D + col, ob);
+      if (ld_ok) tmem_wait_ld();
       if (row_ok) {
         uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          w[i] = have_o ? pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv)
-                        : 0u;
+        for (int i = 0; i < 16; ++i) {
+          float x0 = 0.f, x1 = 0.f;
+          if (good) {
+            if (use_a) {
+              x0 = __uint_as_float(oa[2 * i]) * fa;
+              x1 = __uint_as_float(oa[2 * i + 1]) * fa;
+            }
+            if (use_b) {
+              x0 = fmaf(__uint_as_float(ob[2 * i]), fb, x0);
+              x1 = fmaf(__uint_as_float(ob[2 * i + 1]), fb, x1);
+            }
+          }
+          w[i] = pack_bf16x2(x0, x1);
+        }
         uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
 #pragma unroll
         for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
       }
     }
-    if (row_ok && a.lse)
-      a.lse[bh * a.S + qpos] = (have_o && l > 0.f) ? (m_ref + log2f(l)) * kLn2 : -INFINITY;
+    if (row_ok && wg == 0 && a.lse)
+      a.lse[bh * a.S + qpos] = good ? (m + log2f(lt)) * kLn2 : -INFINITY;
   }
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 1) {
+  if (warp == 2) {
     tc_fence_after();
     if (lane == 0) drain_wait(fin, 0, 1000000000ull);   // every MMA retired before TMEM is freed
     __syncwarp();
@@ -537,7 +659,7 @@ cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
   a.H_kv = pa.H_kv;
   a.max_blk = pa.max_blk;
   a.max_col = pa.max_col;
-  a.n_qblk = (pa.S + 63) / 64;
+  a.n_qblk = (pa.S + kBlk - 1) / kBlk;
   a.n_words = (a.n_qblk + 31) / 32;
   a.sl2 = pa.scale * kLog2e;
   static std::atomic<int> epoch{0};
@@ -558,9 +680,12 @@ cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
 
 }  // namespace
 
+// The kernel orders scores by their raw value, which needs a positive scale; it also
+// needs D in {64, 128} and the bitmaps of one query-block pair in shared memory.
 bool prefill_tc_supported(const PrefillArgs &a) {
   if (a.D != 64 && a.D != 128) return false;
-  const int n_qblk = (a.S + 63) / 64;
+  if (!(a.scale > 0.f)) return false;
+  const int n_qblk = (a.S + kBlk - 1) / kBlk;
   const size_t smem = a.D == 128 ? Layout<128>::bytes((n_qblk + 31) / 32)
                                  : Layout<64>::bytes((n_qblk + 31) / 32);
   return smem <= 227 * 1024 && encode_fn() != nullptr;

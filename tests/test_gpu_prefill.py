@@ -217,8 +217,11 @@ def test_tensor_core_and_warp_mma_kernels_agree(D):
         o_tc, l_tc = dsa.sparse_attn_prefill(q, k, v, *lists)
         o_mm, l_mm = _with_impl("mma", lambda: dsa.sparse_attn_prefill(q, k, v, *lists))
         torch.cuda.synchronize()
+        # two bf16 outputs: each is checked against the oracle elsewhere; here allow the
+        # oracle tolerance plus one bf16 ulp (2^-7 relative) for adjacent roundings
         d = (o_tc.float() - o_mm.float()).abs()
-        assert d.max().item() <= MAX_ABS and d.mean().item() <= MEAN_ABS
+        assert (d <= MAX_ABS + o_mm.float().abs() * 2.0 ** -7).all()
+        assert d.mean().item() <= MEAN_ABS
         fin = torch.isfinite(l_mm)
         assert torch.equal(fin, torch.isfinite(l_tc))
         assert (l_tc[fin] - l_mm[fin]).abs().max().item() <= 1e-3
