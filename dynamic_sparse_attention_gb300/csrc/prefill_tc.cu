@@ -14,24 +14,25 @@
 // (descending, so the running max settles early), then block m0's gathered column tiles
 // (128 columns each), then block m1's; a row masks the 64-key halves its own query
 // block does not list, keys after it (causal) and keys past the sequence end.
-// Warp roles (352 threads):
+// Warp roles (608 threads):
 //   warp 0     K producer: Q once (TMA), then K tiles (TMA for block tiles, 16-byte
 //              cp.async gathers for column tiles) into a 3-stage ring; writes each
 //              tile's description (kind, key tile, per-half membership, positions);
 //   warp 1     V producer: V tiles into a 2-stage ring (its own walk of the same list);
-//   warp 2     MMA issuer (one thread): S_x = Q K^T (M = N = 128, K = D) into TMEM, then
-//              O_x += P V (A = P read from TMEM, 128 keys), x = tile parity;
-//   warps 3-10 softmax: two independent warpgroups; warpgroup x owns the tiles of
-//              parity x (S_x, O_x, its running max and row sum), one thread per query
-//              row (warp w reads the TMEM lanes of quarter w % 4).  Pass 1 takes the
-//              masked row max; pass 2 forms P = exp2(s * scale * log2e - max) with the
-//              exact running max of the stream (its largest probability is exactly 1,
-//              free of bf16 rounding) and writes P as bf16 pairs over the first 64
-//              columns of S_x, where the P V MMA reads it.  O_x is brought to the
-//              stream's current max before P is released (the stream's previous P V
-//              retired before the Q K^T that filled S_x, as one thread issues both in
-//              order).  The epilogue merges the two streams (log-sum-exp), normalises
-//              and stores.
+//   warp 2     MMA issuer (one thread): S_b = Q K^T (M = N = 128, K = D) into one of three
+//              TMEM score buffers (b = tile mod 3), O += P V (A = P read from TMEM,
+//              128 keys).  Q K^T of tile t + 3 is queued right behind P V of tile t, so
+//              the scores of the next two tiles are ready while tile t is in softmax;
+//   warps 3-18 softmax: four threads per query row; warp w reads the TMEM lanes of
+//              quarter w % 4 and one 32-key slice of the tile.  The four slices of a
+//              row combine their maxima through shared memory (a named barrier per lane
+//              quarter); each thread then forms P = exp2(s * scale * log2e - max) with the
+//              exact running max (the row's largest probability is exactly 1, free of
+//              bf16 rounding), keeps a partial row sum, and writes its 16 bf16 pairs over
+//              the first 64 columns of S_b, where the P V MMA reads them.  When the max
+//              grows, each warp brings its quarter of O to the new max once P V of the
+//              previous tile has retired.  The epilogue adds the partial sums,
+//              normalises and stores.
 // Operands: Q and K tiles are K-major with 128-byte swizzle (what TMA writes for a
 // 64-element-wide box); V tiles are the B operand in MN-major form (keys along K).
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work, drains its
@@ -63,8 +64,10 @@ constexpr int kBlk = 64;           // block size of the tile lists
 constexpr int kKeys = 128;         // keys per MMA tile (two list blocks)
 constexpr int kKS = 3;             // K ring stages
 constexpr int kVS = 2;             // V ring stages
+constexpr int kSB = 3;             // TMEM score buffers
 constexpr int kMetaRing = 8;       // tile descriptions in flight (the K ring runs at most 6 ahead)
-constexpr int kThreads = 11 * 32;  // K producer, V producer, MMA issuer, 8 softmax warps
+constexpr int kSmWarps = 16;       // softmax warps: 4 lane quarters x 4 key slices
+constexpr int kThreads = (3 + kSmWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -93,14 +96,15 @@ struct Layout {
   static constexpr uint32_t oV = oK + kKS * kTile;
   static constexpr uint32_t oMeta = oV + kVS * kTile;
   static constexpr uint32_t oBar = oMeta + kMetaRing * sizeof(TileMeta);
-  static constexpr int kBars = 2 * kKS + 2 * kVS + 9;
+  static constexpr int kBars = 2 * kKS + 2 * kVS + 3 * kSB + 2;
   static constexpr uint32_t oMisc = oBar + kBars * 8;
-  static constexpr uint32_t oXch = oMisc + 64;              // [2 streams][128 rows] x (max, sum)
-  static constexpr uint32_t oBits = oXch + 2048;
+  static constexpr uint32_t oRed = oMisc + 64;              // [3][4 slices][128 rows] floats
+  static constexpr uint32_t oOk = oRed + 3 * 4 * kRowsQ * 4;   // [3][4 quarters][4 slices] ints
+  static constexpr uint32_t oBits = oOk + 3 * 16 * 4;
   static size_t bytes(int n_words) { return oBits + 8ull * n_words + 1024; }
-  // TMEM columns (32-bit): S_0, S_1 (P_x over the first 64 columns of S_x) | O_0, O_1
-  static constexpr uint32_t cO = 2 * kKeys;
-  static_assert(cO + 2 * D <= kTmemCols, "TMEM columns");
+  // TMEM columns (32-bit): S_0, S_1, S_2 (P_b over the first 64 columns of S_b) | O
+  static constexpr uint32_t cO = kSB * kKeys;
+  static_assert(cO + D <= kTmemCols, "TMEM columns");
   static_assert(oQ % 1024 == 0 && oK % 1024 == 0 && oV % 1024 == 0, "swizzle atoms");
 };
 
@@ -201,8 +205,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
   uint64_t *k_full = bars, *k_empty = k_full + kKS;
   uint64_t *v_full = k_empty + kKS, *v_empty = v_full + kVS;
-  uint64_t *s_full = v_empty + kVS, *p_full = s_full + 2, *pv_done = p_full + 2;
-  uint64_t *q_full = pv_done + 2, *fin = q_full + 1, *xfin = fin + 1;
+  uint64_t *s_full = v_empty + kVS, *p_full = s_full + kSB;
+  uint64_t *pv_done = p_full + kSB, *q_full = pv_done + kSB, *fin = q_full + 1;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::oMisc + 4);
   int *n_blk_tiles_s = reinterpret_cast<int *>(sm + L::oMisc + 8);
@@ -222,15 +226,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 
   if (tid == 0) {
     for (int i = 0; i < 2 * kKS + 2 * kVS; ++i) mbar_init(&bars[i], 1);
-    mbar_init(&s_full[0], 1);
-    mbar_init(&s_full[1], 1);
-    mbar_init(&p_full[0], 4);     // one arrival per softmax warp of the stream
-    mbar_init(&p_full[1], 4);
-    mbar_init(&pv_done[0], 1);
-    mbar_init(&pv_done[1], 1);
+    for (int i = 0; i < kSB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kSmWarps);   // one arrival per softmax warp
+      mbar_init(&pv_done[i], 1);
+    }
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
-    mbar_init(xfin, 8);           // one arrival per softmax warp
     *abort_flag = 0;
     *n_blk_tiles_s = 0;
     fence_mbar_init();
@@ -378,12 +380,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const uint32_t sQ = smem_u32(sm + L::oQ);
       const uint32_t sK = smem_u32(sm + L::oK);
       const uint32_t sV = smem_u32(sm + L::oV);
-      bool ok = tc_wait(q_full, 0, wc);
       auto issue_qk = [&](int t) -> bool {
         const int st = t % kKS;
         if (!tc_wait(&k_full[st], (t / kKS) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t d = tmem + static_cast<uint32_t>((t & 1) * kKeys);
+        const uint32_t d = tmem + static_cast<uint32_t>((t % kSB) * kKeys);
         const uint32_t kbase = sK + st * L::kTile;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
@@ -391,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           const uint64_t bd = sdesc_sw128(kbase + (kk >> 2) * L::kHalf + (kk & 3) * 32, 16, 1024);
           tc_mma(d, ad, bd, id_qk, kk > 0 ? 1u : 0u);
         }
-        tc_commit(&s_full[t & 1]);
+        tc_commit(&s_full[t % kSB]);
         tc_commit(&k_empty[st]);
         return true;
       };
@@ -400,199 +401,188 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         if (!tc_wait(&v_full[st], (t / kVS) & 1, wc)) return false;
         tc_fence_after();
         const uint32_t vbase = sV + st * L::kTile;
-        const uint32_t pcol = tmem + static_cast<uint32_t>((t & 1) * kKeys);
-        const uint32_t ocol = tmem + L::cO + static_cast<uint32_t>((t & 1) * D);
+        const uint32_t pcol = tmem + static_cast<uint32_t>((t % kSB) * kKeys);
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk) {
           const uint64_t bd = sdesc_sw128(vbase + kk * 2048, L::kHalf, 1024);
-          tc_mma_ts(ocol, pcol + kk * 8, bd, id_pv, (t >= 2 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + L::cO, pcol + kk * 8, bd, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
         }
-        tc_commit(&pv_done[t & 1]);
+        tc_commit(&pv_done[t % kSB]);
         tc_commit(&v_empty[st]);
         return true;
       };
-      if (ok && T > 0) ok = issue_qk(0);
+      // Q K^T runs kSB tiles ahead; Q K^T of tile t + kSB reuses S_b right behind P V of t
+      bool ok = tc_wait(q_full, 0, wc);
+      for (int t = 0; ok && t < min(T, kSB); ++t) ok = issue_qk(t);
       for (int t = 0; ok && t < T; ++t) {
-        if (t + 1 < T && !(ok = issue_qk(t + 1))) break;
-        if (!(ok = tc_wait(&p_full[t & 1], (t >> 1) & 1, wc))) break;
+        if (!(ok = tc_wait(&p_full[t % kSB], (t / kSB) & 1, wc))) break;
         tc_fence_after();
-        ok = issue_pv(t);
+        if (!(ok = issue_pv(t))) break;
+        if (t + kSB < T) ok = issue_qk(t + kSB);
       }
       tc_commit(fin);
     }
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
-    const int wg = (warp - 3) >> 2;   // stream: tiles t with t % 2 == wg
-    const int quarter = warp & 3;
+    const int sw = warp - 3;
+    const int quarter = warp & 3;      // TMEM lanes this warp may access
+    const int cs = sw >> 2;            // 32-key slice of each tile
     const int row = quarter * 32 + lane;
     const int grp = row >> 6;
     const int qpos = kRowsQ * p + row;
     const bool row_ok = qpos < a.S;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const uint32_t s_col = tl + static_cast<uint32_t>(wg * kKeys);   // S_wg (P_wg over its start)
-    const uint32_t o_col = tl + L::cO + static_cast<uint32_t>(wg * D);
+    constexpr int kOS = D / 4;         // O columns this warp rescales and stores
+    const uint32_t o_col = tl + L::cO + static_cast<uint32_t>(cs * kOS);
+    float *red = reinterpret_cast<float *>(sm + L::oRed);   // [3][4][128]
+    int *okw = reinterpret_cast<int *>(sm + L::oOk);        // [3][4][4]
+    const uint32_t bar_id = 1u + static_cast<uint32_t>(quarter);   // the row quarter's 4 warps
     const float sl2 = a.sl2;
-    const int last_key = min(qpos, a.S - 1);   // causal and in-sequence bound of the row
-    float m_cur = -INFINITY, l = 0.f;   // stream's running max (base-2 units) and row sum
-    float m_o = -INFINITY;              // max that O_wg is currently relative to
-    bool ok = true;
     const float2 sl2x2 = make_float2(sl2, sl2);
-    for (int t = wg; t < T; t += 2) {
-      if (!(ok = warp_wait(&s_full[wg], (t >> 1) & 1, wc))) break;
-      tc_fence_after();
-      const TileMeta *md = &meta[t % kMetaRing];
-      const int kind = md->kind;
-      const int hmask = row_ok ? (md->mask >> (2 * grp)) & 3 : 0;   // halves this row uses
-      const int lim = last_key - kKeys * md->n;   // block tile: slots c <= lim are the row's keys
-      const bool trim = kind != 0 || hmask != 3 || lim < kKeys - 1;   // some slot is not the row's
-      // -inf over the slots [c0, c0 + N) that are not keys of this row
-      auto mask_slots = [&](uint32_t *v, const int c0, const int N) {
+    const int last_key = min(qpos, a.S - 1);   // causal and in-sequence bound of the row
+    float m_cur = -INFINITY, l = 0.f;   // running max (base-2 units), this slice's row sum
+    float m_o = -INFINITY;              // max that O is currently relative to
+    bool ok = true;
+    int sb = 0;                         // t % kSB
+    for (int t = 0; t < T; ++t) {
+      const uint32_t s_col = tl + static_cast<uint32_t>(sb * kKeys);
+      const bool got = warp_wait(&s_full[sb], (t / kSB) & 1, wc);
+      float lmax = -INFINITY;
+      uint32_t s[32];
+      if (got) {
+        tc_fence_after();
+        tmem_ld32(s_col + 32 * cs, s);
+        const TileMeta *md = &meta[t % kMetaRing];
+        const int kind = md->kind;
+        const int hmask = row_ok ? (md->mask >> (2 * grp)) & 3 : 0;   // halves this row uses
+        const int lim = last_key - kKeys * md->n - 32 * cs;   // block tile: slot c <= lim is a key
+        tmem_wait_ld();
         if (kind == 0) {
+          if (!((hmask >> (cs >> 1)) & 1)) {
 #pragma unroll
-          for (int c = 0; c < N; ++c)
-            if (!((hmask >> ((c0 + c) >> 6)) & 1) || c0 + c > lim) v[c] = __float_as_uint(-INFINITY);
+            for (int c = 0; c < 32; ++c) s[c] = __float_as_uint(-INFINITY);
+          } else if (lim < 31) {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (c > lim) s[c] = __float_as_uint(-INFINITY);
+          }
         } else {
-          const int4 *pp = reinterpret_cast<const int4 *>(md->pos + c0);
+          const int4 *pp = reinterpret_cast<const int4 *>(md->pos + 32 * cs);
 #pragma unroll
-          for (int c4 = 0; c4 < N / 4; ++c4) {
+          for (int c4 = 0; c4 < 8; ++c4) {
             const int4 j = pp[c4];
-            if (hmask == 0 || j.x < 0 || j.x > qpos) v[4 * c4] = __float_as_uint(-INFINITY);
-            if (hmask == 0 || j.y < 0 || j.y > qpos) v[4 * c4 + 1] = __float_as_uint(-INFINITY);
-            if (hmask == 0 || j.z < 0 || j.z > qpos) v[4 * c4 + 2] = __float_as_uint(-INFINITY);
-            if (hmask == 0 || j.w < 0 || j.w > qpos) v[4 * c4 + 3] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.x < 0 || j.x > qpos) s[4 * c4] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.y < 0 || j.y > qpos) s[4 * c4 + 1] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.z < 0 || j.z > qpos) s[4 * c4 + 2] = __float_as_uint(-INFINITY);
+            if (hmask == 0 || j.w < 0 || j.w > qpos) s[4 * c4 + 3] = __float_as_uint(-INFINITY);
           }
         }
-      };
-      // pass 1, 64 keys at a time: masked row max of the tile (four max chains)
-      float mx[4];
+        float mx[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t s[64];
-        tmem_ld32(s_col + 64 * hf, s);
-        tmem_ld32(s_col + 64 * hf + 32, s + 32);
-        tmem_wait_ld();
-        if (trim) mask_slots(s, 64 * hf, 64);
-#pragma unroll
-        for (int c = 0; c < 64; c += 2)
+        for (int c = 0; c < 32; c += 2)
           mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
+        lmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       }
-      const float mt = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3])) * sl2;   // sl2 > 0 keeps the order
-      if (mt > m_cur) {
+      // combine the four slices of each row; every warp of the quarter takes the same
+      // branch below, so all four reach every barrier of the quarter
+      const int x = t & 1;
+      red[(x * 4 + cs) * kRowsQ + row] = lmax;
+      if (lane == 0) okw[(x * 4 + quarter) * 4 + cs] = got ? 1 : 0;
+      named_bar_sync(bar_id, 128);
+      const int *okq = okw + (x * 4 + quarter) * 4;
+      if (!(okq[0] & okq[1] & okq[2] & okq[3])) {
+        ok = false;
+        break;
+      }
+      const float *rr = red + x * 4 * kRowsQ + row;
+      const float mt = fmax3(rr[0], rr[kRowsQ], fmaxf(rr[2 * kRowsQ], rr[3 * kRowsQ])) * sl2;
+      if (mt > m_cur) {   // sl2 > 0: same order as the scaled scores
         if (m_cur != -INFINITY) l *= fast_exp2(m_cur - mt);
         m_cur = mt;
       }
-      // pass 2, 64 keys at a time: probabilities -> bf16 pairs over the first 64 columns
-      // of S_wg (half hf lands on columns 32hf..32hf+31, which pass 2 has already read)
-      const float nm = m_cur == -INFINITY ? 0.f : -m_cur;   // no key yet: every s is -inf
-      const float2 nm2 = make_float2(nm, nm);
-      float2 acc[4];
+      // probabilities -> 16 bf16 pairs at columns 16cs..16cs+15 of S_b (their scores are
+      // in registers of this quarter's warps, all loaded before the barrier)
+      {
+        const float nm = m_cur == -INFINITY ? 0.f : -m_cur;   // no key yet: every s is -inf
+        const float2 nm2 = make_float2(nm, nm);
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        uint32_t pk[16];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) acc[i] = make_float2(0.f, 0.f);
-#pragma unroll
-      for (int hf = 0; hf < 2; ++hf) {
-        uint32_t s[64], pk[32];
-        tmem_ld32(s_col + 64 * hf, s);
-        tmem_ld32(s_col + 64 * hf + 32, s + 32);
-        tmem_wait_ld();
-        if (trim) mask_slots(s, 64 * hf, 64);
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) {
-          const float2 x = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nm2);
-          const float2 e = make_float2(fast_exp2(x.x), fast_exp2(x.y));
-          acc[(c >> 1) & 3] = fadd2(acc[(c >> 1) & 3], e);
+        for (int c = 0; c < 32; c += 2) {
+          const float2 y = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nm2);
+          const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+          if ((c >> 1) & 1) acc1 = fadd2(acc1, e);
+          else acc0 = fadd2(acc0, e);
           pk[c >> 1] = pack_bf16x2(e.x, e.y);
         }
-        tmem_st32(s_col + 32 * hf, pk);
+        tmem_st16(s_col + 16 * cs, pk);
+        const float2 as = fadd2(acc0, acc1);
+        l += as.x + as.y;
       }
-      const float2 a01 = fadd2(fadd2(acc[0], acc[1]), fadd2(acc[2], acc[3]));
-      l += a01.x + a01.y;
-      // O_wg to the current max.  The stream's previous P V has retired: the Q K^T that
-      // filled S_wg was issued after it by the same thread and completes after it.
+      // O to the current max, once P V of the previous tile has retired.  P V of tile k
+      // completes phase k / 3 of pv_done[k % 3]; P V of tile t - 4 has retired (Q K^T of
+      // tile t came after it), so the parity names the phase of tile t - 1 exactly.
       const bool stale = m_o != -INFINITY && m_o < m_cur;
       if (__any_sync(kFull, stale)) {
-        const float f = stale ? fast_exp2(m_o - m_cur) : 1.f;
-        const float2 f2 = make_float2(f, f);
-#pragma unroll 1
-        for (int ch = 0; ch < D / 32; ++ch) {
-          uint32_t o[32];
-          tmem_ld32(o_col + ch * 32, o);
+        const int tp = t - 1;   // >= 0: O has a max only after a tile
+        if (warp_wait(&pv_done[tp % kSB], (tp / kSB) & 1, wc)) {
+          tc_fence_after();
+          const float f = stale ? fast_exp2(m_o - m_cur) : 1.f;
+          const float2 f2 = make_float2(f, f);
+          uint32_t o[kOS];
+          if constexpr (kOS == 32) tmem_ld32(o_col, o);
+          else tmem_ld16(o_col, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < 32; i += 2) {
+          for (int i = 0; i < kOS; i += 2) {
             const float2 y = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2);
             o[i] = __float_as_uint(y.x);
             o[i + 1] = __float_as_uint(y.y);
           }
-          tmem_st32(o_col + ch * 32, o);
+          if constexpr (kOS == 32) tmem_st32(o_col, o);
+          else tmem_st16(o_col, o);
         }
       }
       m_o = m_cur;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[wg]);
+      if (lane == 0) mbar_arrive(&p_full[sb]);
+      sb = sb + 1 == kSB ? 0 : sb + 1;
     }
-    // this stream's last P V, if it has tiles
-    const bool mine = T > wg;
-    const int t_last = mine ? wg + 2 * ((T - 1 - wg) >> 1) : 0;
-    if (ok && mine) ok = warp_wait(&pv_done[wg], (t_last >> 1) & 1, wc);
-    // publish (max, sum) of this stream; read the other one
-    float *xch = reinterpret_cast<float *>(sm + L::oXch);
-    xch[(wg * kRowsQ + row) * 2] = (ok && mine) ? m_cur : -INFINITY;
-    xch[(wg * kRowsQ + row) * 2 + 1] = (ok && mine) ? l : 0.f;
-    __syncwarp();
-    if (lane == 0) mbar_arrive(xfin);
-    const bool have_x = warp_wait(xfin, 0, wc);
-    tc_fence_after();
-    const float ma = xch[row * 2], la = xch[row * 2 + 1];
-    const float mb = xch[(kRowsQ + row) * 2], lb = xch[(kRowsQ + row) * 2 + 1];
-    const float m = fmaxf(ma, mb);
-    const float wa = (ma != -INFINITY) ? exp2f(ma - m) : 0.f;
-    const float wb = (mb != -INFINITY) ? exp2f(mb - m) : 0.f;
-    const float lt = la * wa + lb * wb;
-    // both streams' accumulators are final once every softmax warp has published
-    const bool ld_ok = have_x && ok;   // warp-uniform: the TMEM loads are collective
+    // epilogue: the last P V, then the row sums of the four slices
+    const bool have_o = ok && T > 0 && warp_wait(&pv_done[(T - 1) % kSB], ((T - 1) / kSB) & 1, wc);
+    red[(2 * 4 + cs) * kRowsQ + row] = l;
+    if (lane == 0) okw[(2 * 4 + quarter) * 4 + cs] = (ok && (T == 0 || have_o)) ? 1 : 0;
+    named_bar_sync(bar_id, 128);
+    const int *okq = okw + (2 * 4 + quarter) * 4;
+    const bool all_ok = okq[0] & okq[1] & okq[2] & okq[3];
+    const float *rr = red + 2 * 4 * kRowsQ + row;
+    const float lt = (rr[0] + rr[kRowsQ]) + (rr[2 * kRowsQ] + rr[3 * kRowsQ]);
+    const bool ld_ok = all_ok && T > 0;   // warp-uniform: the TMEM load is collective
     const bool good = ld_ok && lt > 0.f;
     const float inv = good ? 1.f / lt : 0.f;
-    const float fa = wa * inv, fb = wb * inv;
-    const bool use_a = T > 0, use_b = T > 1;
-    // stream wg writes columns [wg * D/2, (wg + 1) * D/2) of the output row
-    uint16_t *orow = a.out + ((static_cast<size_t>(b) * a.S + (row_ok ? qpos : 0)) * a.H_q + h) * D +
-                     wg * (D / 2);
-#pragma unroll 1
-    for (int ch = 0; ch < D / 64; ++ch) {
-      uint32_t oa[32], ob[32];
-      const uint32_t col = static_cast<uint32_t>(wg * (D / 2) + ch * 32);
-      if (ld_ok && use_a) tmem_ld32(tl + L::cO + col, oa);
-      if (ld_ok && use_b) tmem_ld32(tl + L::cO + D + col, ob);
-      if (ld_ok) tmem_wait_ld();
-      if (row_ok) {
-        uint32_t w[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          float x0 = 0.f, x1 = 0.f;
-          if (good) {
-            if (use_a) {
-              x0 = __uint_as_float(oa[2 * i]) * fa;
-              x1 = __uint_as_float(oa[2 * i + 1]) * fa;
-            }
-            if (use_b) {
-              x0 = fmaf(__uint_as_float(ob[2 * i]), fb, x0);
-              x1 = fmaf(__uint_as_float(ob[2 * i + 1]), fb, x1);
-            }
-          }
-          w[i] = pack_bf16x2(x0, x1);
-        }
-        uint4 *dst = reinterpret_cast<uint4 *>(orow + ch * 32);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      }
+    uint32_t o[kOS];
+    if (ld_ok) {
+      tc_fence_after();
+      if constexpr (kOS == 32) tmem_ld32(o_col, o);
+      else tmem_ld16(o_col, o);
+      tmem_wait_ld();
     }
-    if (row_ok && wg == 0 && a.lse)
-      a.lse[bh * a.S + qpos] = good ? (m + log2f(lt)) * kLn2 : -INFINITY;
+    if (row_ok) {
+      uint32_t w[kOS / 2];
+#pragma unroll
+      for (int i = 0; i < kOS / 2; ++i)
+        w[i] = good ? pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv) : 0u;
+      uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((static_cast<size_t>(b) * a.S + qpos) * a.H_q + h) * D +
+                                             cs * kOS);
+#pragma unroll
+      for (int i = 0; i < kOS / 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      if (cs == 0 && a.lse) a.lse[bh * a.S + qpos] = good ? (m_cur + log2f(lt)) * kLn2 : -INFINITY;
+    }
   }
 
   tc_fence_before();
