@@ -66,7 +66,9 @@ constexpr int kKS = 3;             // K ring stages
 constexpr int kVS = 2;             // V ring stages
 constexpr int kSB = 3;             // TMEM score buffers
 constexpr int kMetaRing = 8;       // tile descriptions in flight (the K ring runs at most 6 ahead)
-constexpr int kSmWarps = 16;       // softmax warps: 4 lane quarters x 4 key slices
+constexpr int kSlices = 2;         // key slices per query row (threads per row)
+constexpr int kSW = kKeys / kSlices;   // keys per slice
+constexpr int kSmWarps = 4 * kSlices;  // softmax warps: 4 TMEM lane quarters x kSlices
 constexpr int kThreads = (3 + kSmWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -96,11 +98,11 @@ struct Layout {
   static constexpr uint32_t oV = oK + kKS * kTile;
   static constexpr uint32_t oMeta = oV + kVS * kTile;
   static constexpr uint32_t oBar = oMeta + kMetaRing * sizeof(TileMeta);
-  static constexpr int kBars = 2 * kKS + 2 * kVS + 3 * kSB + 2;
+  // rings, score buffers, q_full, fin, then per lane quarter: max exchange x2, sum exchange
+  static constexpr int kBars = 2 * kKS + 2 * kVS + 3 * kSB + 2 + 4 * 3;
   static constexpr uint32_t oMisc = oBar + kBars * 8;
-  static constexpr uint32_t oRed = oMisc + 64;              // [3][4 slices][128 rows] floats
-  static constexpr uint32_t oOk = oRed + 3 * 4 * kRowsQ * 4;   // [3][4 quarters][4 slices] ints
-  static constexpr uint32_t oBits = oOk + 3 * 16 * 4;
+  static constexpr uint32_t oRed = oMisc + 64;              // [3][kSlices][128 rows] floats
+  static constexpr uint32_t oBits = oRed + 3 * kSlices * kRowsQ * 4;
   static size_t bytes(int n_words) { return oBits + 8ull * n_words + 1024; }
   // TMEM columns (32-bit): S_0, S_1, S_2 (P_b over the first 64 columns of S_b) | O
   static constexpr uint32_t cO = kSB * kKeys;
@@ -207,6 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint64_t *v_full = k_empty + kKS, *v_empty = v_full + kVS;
   uint64_t *s_full = v_empty + kVS, *p_full = s_full + kSB;
   uint64_t *pv_done = p_full + kSB, *q_full = pv_done + kSB, *fin = q_full + 1;
+  uint64_t *xbar = fin + 1;   // [4 quarters][3]: row-max exchange by tile parity, row sums
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oMisc);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::oMisc + 4);
   int *n_blk_tiles_s = reinterpret_cast<int *>(sm + L::oMisc + 8);
@@ -233,6 +236,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     }
     mbar_init(q_full, 1);
     mbar_init(fin, 1);
+    for (int i = 0; i < 4 * 3; ++i) mbar_init(&xbar[i], kSlices);   // one arrival per key slice
     *abort_flag = 0;
     *n_blk_tiles_s = 0;
     fence_mbar_init();
@@ -425,151 +429,192 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax + epilogue
+    // Software-pipelined over tiles: the scores of tile t + 1 stream in from TMEM into the
+    // registers that the exponentials of tile t have just consumed (half a slice at a
+    // time), and their slice maximum is published right after P of tile t is released.
     const int sw = warp - 3;
     const int quarter = warp & 3;      // TMEM lanes this warp may access
-    const int cs = sw >> 2;            // 32-key slice of each tile
+    const int cs = sw >> 2;            // key slice of each tile
     const int row = quarter * 32 + lane;
     const int grp = row >> 6;
     const int qpos = kRowsQ * p + row;
     const bool row_ok = qpos < a.S;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    constexpr int kOS = D / 4;         // O columns this warp rescales and stores
+    constexpr int kOS = D / kSlices;   // O columns this warp rescales and stores
     const uint32_t o_col = tl + L::cO + static_cast<uint32_t>(cs * kOS);
-    float *red = reinterpret_cast<float *>(sm + L::oRed);   // [3][4][128]
-    int *okw = reinterpret_cast<int *>(sm + L::oOk);        // [3][4][4]
-    const uint32_t bar_id = 1u + static_cast<uint32_t>(quarter);   // the row quarter's 4 warps
+    float *red = reinterpret_cast<float *>(sm + L::oRed);   // [3][kSlices][128 rows]
+    uint64_t *qbar = xbar + 3 * quarter;   // this quarter's exchange barriers
     const float sl2 = a.sl2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     const int last_key = min(qpos, a.S - 1);   // causal and in-sequence bound of the row
     float m_cur = -INFINITY, l = 0.f;   // running max (base-2 units), this slice's row sum
     float m_o = -INFINITY;              // max that O is currently relative to
     bool ok = true;
-    int sb = 0;                         // t % kSB
-    for (int t = 0; t < T; ++t) {
-      const uint32_t s_col = tl + static_cast<uint32_t>(sb * kKeys);
-      const bool got = warp_wait(&s_full[sb], (t / kSB) & 1, wc);
-      float lmax = -INFINITY;
-      uint32_t s[32];
-      if (got) {
-        tc_fence_after();
-        tmem_ld32(s_col + 32 * cs, s);
-        const TileMeta *md = &meta[t % kMetaRing];
-        const int kind = md->kind;
-        const int hmask = row_ok ? (md->mask >> (2 * grp)) & 3 : 0;   // halves this row uses
-        const int lim = last_key - kKeys * md->n - 32 * cs;   // block tile: slot c <= lim is a key
-        tmem_wait_ld();
-        if (kind == 0) {
-          if (!((hmask >> (cs >> 1)) & 1)) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c) s[c] = __float_as_uint(-INFINITY);
-          } else if (lim < 31) {
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-              if (c > lim) s[c] = __float_as_uint(-INFINITY);
+    uint32_t sc[kSW];                   // this slice's scores (then those of the next tile)
+
+    // TMEM column of 32-column part i of this slice in score buffer t % 3
+    auto s_addr = [&](int t, int i) {
+      return tl + static_cast<uint32_t>((t % kSB) * kKeys + kSW * cs + 32 * i);
+    };
+    // mask the scores of tile t once loaded, publish this slice's maximum
+    auto publish_max = [&](int t) {
+      const TileMeta *md = &meta[t % kMetaRing];
+      const int kind = md->kind;
+      const int hmask = row_ok ? (md->mask >> (2 * grp)) & 3 : 0;   // halves this row uses
+      uint32_t valid = 0u;   // bit c: slot c of a 32-slot part is a key of the row
+      int lim = 0;
+      if (kind == 0) {
+        // a slice lies inside one 64-key half: key kSW * cs + c is in half (kSW * cs) / 64
+        const bool member = (hmask >> ((kSW * cs) >> 6)) & 1;
+        lim = member ? last_key - kKeys * md->n - kSW * cs : -1;   // slots <= lim are keys
+      }
+      tmem_wait_ld();
+      const bool trim = kind != 0 || lim < kSW - 1;
+      if (__any_sync(kFull, trim)) {
+#pragma unroll 1
+        for (int i = 0; i < kSW / 32; ++i) {
+          if (kind == 0) {
+            const int li = lim - 32 * i;
+            valid = li < 0 ? 0u : (li >= 31 ? 0xffffffffu : (2u << li) - 1u);
+          } else {
+            valid = 0u;
+            const int4 *pp = reinterpret_cast<const int4 *>(md->pos + kSW * cs + 32 * i);
+#pragma unroll 1
+            for (int c4 = 0; c4 < 8; ++c4) {
+              const int4 j = pp[c4];
+              valid |= (static_cast<uint32_t>(j.x >= 0 && j.x <= qpos) << (4 * c4)) |
+                       (static_cast<uint32_t>(j.y >= 0 && j.y <= qpos) << (4 * c4 + 1)) |
+                       (static_cast<uint32_t>(j.z >= 0 && j.z <= qpos) << (4 * c4 + 2)) |
+                       (static_cast<uint32_t>(j.w >= 0 && j.w <= qpos) << (4 * c4 + 3));
+            }
+            if (hmask == 0) valid = 0u;
           }
-        } else {
-          const int4 *pp = reinterpret_cast<const int4 *>(md->pos + 32 * cs);
 #pragma unroll
-          for (int c4 = 0; c4 < 8; ++c4) {
-            const int4 j = pp[c4];
-            if (hmask == 0 || j.x < 0 || j.x > qpos) s[4 * c4] = __float_as_uint(-INFINITY);
-            if (hmask == 0 || j.y < 0 || j.y > qpos) s[4 * c4 + 1] = __float_as_uint(-INFINITY);
-            if (hmask == 0 || j.z < 0 || j.z > qpos) s[4 * c4 + 2] = __float_as_uint(-INFINITY);
-            if (hmask == 0 || j.w < 0 || j.w > qpos) s[4 * c4 + 3] = __float_as_uint(-INFINITY);
-          }
+          for (int c = 0; c < 32; ++c)
+            if (i == 0) sc[c] = (valid >> c) & 1u ? sc[c] : __float_as_uint(-INFINITY);
+            else if (kSW > 32) sc[32 + c] = (valid >> c) & 1u ? sc[32 + c] : __float_as_uint(-INFINITY);
         }
-        float mx[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 32; c += 2)
-          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(s[c]), __uint_as_float(s[c + 1]));
-        lmax = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
       }
-      // combine the four slices of each row; every warp of the quarter takes the same
-      // branch below, so all four reach every barrier of the quarter
-      const int x = t & 1;
-      red[(x * 4 + cs) * kRowsQ + row] = lmax;
-      if (lane == 0) okw[(x * 4 + quarter) * 4 + cs] = got ? 1 : 0;
-      named_bar_sync(bar_id, 128);
-      const int *okq = okw + (x * 4 + quarter) * 4;
-      if (!(okq[0] & okq[1] & okq[2] & okq[3])) {
-        ok = false;
-        break;
-      }
-      const float *rr = red + x * 4 * kRowsQ + row;
-      const float mt = fmax3(rr[0], rr[kRowsQ], fmaxf(rr[2 * kRowsQ], rr[3 * kRowsQ])) * sl2;
+      float mx[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+#pragma unroll
+      for (int c = 0; c < kSW; c += 2)
+        mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sc[c]), __uint_as_float(sc[c + 1]));
+      red[((t & 1) * kSlices + cs) * kRowsQ + row] = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qbar[t & 1]);
+    };
+    // tile t: row max from the row's slices, P, row sum, prefetch of tile t + 1's scores,
+    // rescale, release of P
+    auto finish_tile = [&](int t) -> bool {
+      const bool more = t + 1 < T;
+      // tile t's phase on its exchange barrier is its (t / 2)-th; the warp itself waited
+      // the one before, and the one after needs this warp's own arrival
+      if (!warp_wait(&qbar[t & 1], (t >> 1) & 1, wc)) return false;
+      const float *rr = red + (t & 1) * kSlices * kRowsQ + row;
+      float mraw = rr[0];
+#pragma unroll
+      for (int i = 1; i < kSlices; ++i) mraw = fmaxf(mraw, rr[i * kRowsQ]);
+      const float mt = mraw * sl2;
       if (mt > m_cur) {   // sl2 > 0: same order as the scaled scores
         if (m_cur != -INFINITY) l *= fast_exp2(m_cur - mt);
         m_cur = mt;
       }
-      // probabilities -> 16 bf16 pairs at columns 16cs..16cs+15 of S_b (their scores are
-      // in registers of this quarter's warps, all loaded before the barrier)
-      {
-        const float nm = m_cur == -INFINITY ? 0.f : -m_cur;   // no key yet: every s is -inf
-        const float2 nm2 = make_float2(nm, nm);
-        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      // probabilities -> kSW / 2 bf16 pairs at columns (kSW / 2) cs.. of S_b, the first
+      // half of the tile's score columns; every slice of the tile was loaded before its
+      // maximum was published
+      const float nm = m_cur == -INFINITY ? 0.f : -m_cur;   // no key yet: every s is -inf
+      const float2 nm2 = make_float2(nm, nm);
+      float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+      const uint32_t pcol = tl + static_cast<uint32_t>((t % kSB) * kKeys + (kSW / 2) * cs);
+      bool got = true;
+#pragma unroll
+      for (int i = 0; i < kSW / 32; ++i) {
         uint32_t pk[16];
 #pragma unroll
         for (int c = 0; c < 32; c += 2) {
-          const float2 y = ffma2(make_float2(__uint_as_float(s[c]), __uint_as_float(s[c + 1])), sl2x2, nm2);
+          const int k = 32 * i + c;
+          const float2 y = ffma2(make_float2(__uint_as_float(sc[k]), __uint_as_float(sc[k + 1])), sl2x2, nm2);
           const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
           if ((c >> 1) & 1) acc1 = fadd2(acc1, e);
           else acc0 = fadd2(acc0, e);
           pk[c >> 1] = pack_bf16x2(e.x, e.y);
         }
-        tmem_st16(s_col + 16 * cs, pk);
-        const float2 as = fadd2(acc0, acc1);
-        l += as.x + as.y;
+        tmem_st16(pcol + 16 * i, pk);
+        if (more) {   // part i of this slice is free: bring in tile t + 1's
+          if (i == 0) {
+            got = warp_wait(&s_full[(t + 1) % kSB], ((t + 1) / kSB) & 1, wc);
+            if (got) tc_fence_after();
+          }
+          if (got) tmem_ld32(s_addr(t + 1, i), sc + 32 * i);
+        }
       }
+      const float2 as = fadd2(acc0, acc1);
+      l += as.x + as.y;
       // O to the current max, once P V of the previous tile has retired.  P V of tile k
       // completes phase k / 3 of pv_done[k % 3]; P V of tile t - 4 has retired (Q K^T of
       // tile t came after it), so the parity names the phase of tile t - 1 exactly.
       const bool stale = m_o != -INFINITY && m_o < m_cur;
       if (__any_sync(kFull, stale)) {
         const int tp = t - 1;   // >= 0: O has a max only after a tile
-        if (warp_wait(&pv_done[tp % kSB], (tp / kSB) & 1, wc)) {
-          tc_fence_after();
-          const float f = stale ? fast_exp2(m_o - m_cur) : 1.f;
-          const float2 f2 = make_float2(f, f);
-          uint32_t o[kOS];
-          if constexpr (kOS == 32) tmem_ld32(o_col, o);
-          else tmem_ld16(o_col, o);
+        if (!warp_wait(&pv_done[tp % kSB], (tp / kSB) & 1, wc)) return false;
+        tc_fence_after();
+        const float f = stale ? fast_exp2(m_o - m_cur) : 1.f;
+        const float2 f2 = make_float2(f, f);
+#pragma unroll 1
+        for (int c16 = 0; c16 < kOS; c16 += 16) {
+          uint32_t o[16];
+          tmem_ld16(o_col + c16, o);
           tmem_wait_ld();
 #pragma unroll
-          for (int i = 0; i < kOS; i += 2) {
+          for (int i = 0; i < 16; i += 2) {
             const float2 y = fmul2(make_float2(__uint_as_float(o[i]), __uint_as_float(o[i + 1])), f2);
             o[i] = __float_as_uint(y.x);
             o[i + 1] = __float_as_uint(y.y);
           }
-          if constexpr (kOS == 32) tmem_st32(o_col, o);
-          else tmem_st16(o_col, o);
+          tmem_st16(o_col + c16, o);
         }
       }
       m_o = m_cur;
       tmem_wait_st();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[sb]);
-      sb = sb + 1 == kSB ? 0 : sb + 1;
+      if (lane == 0) mbar_arrive(&p_full[t % kSB]);
+      if (!got) return false;
+      if (more) publish_max(t + 1);
+      return true;
+    };
+    if (T > 0) {
+      if (warp_wait(&s_full[0], 0, wc)) {
+        tc_fence_after();
+#pragma unroll
+        for (int i = 0; i < kSW / 32; ++i) tmem_ld32(s_addr(0, i), sc + 32 * i);
+        publish_max(0);
+      } else {
+        ok = false;
+      }
     }
-    // epilogue: the last P V, then the row sums of the four slices
+    for (int t = 0; ok && t < T; ++t) ok = finish_tile(t);
+    // epilogue: the last P V, then the row sums of the row's slices
     const bool have_o = ok && T > 0 && warp_wait(&pv_done[(T - 1) % kSB], ((T - 1) / kSB) & 1, wc);
-    red[(2 * 4 + cs) * kRowsQ + row] = l;
-    if (lane == 0) okw[(2 * 4 + quarter) * 4 + cs] = (ok && (T == 0 || have_o)) ? 1 : 0;
-    named_bar_sync(bar_id, 128);
-    const int *okq = okw + (2 * 4 + quarter) * 4;
-    const bool all_ok = okq[0] & okq[1] & okq[2] & okq[3];
-    const float *rr = red + 2 * 4 * kRowsQ + row;
-    const float lt = (rr[0] + rr[kRowsQ]) + (rr[2 * kRowsQ] + rr[3 * kRowsQ]);
-    const bool ld_ok = all_ok && T > 0;   // warp-uniform: the TMEM load is collective
+    red[(2 * kSlices + cs) * kRowsQ + row] = l;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&qbar[2]);
+    const bool have_l = warp_wait(&qbar[2], 0, wc);
+    const float *rr = red + 2 * kSlices * kRowsQ + row;
+    float lt = rr[0];
+#pragma unroll
+    for (int i = 1; i < kSlices; ++i) lt += rr[i * kRowsQ];
+    // warp-uniform: the TMEM load is collective.  A CTA that gave up stores zeros.
+    const bool ld_ok = have_o && have_l && !*abort_flag;
     const bool good = ld_ok && lt > 0.f;
     const float inv = good ? 1.f / lt : 0.f;
     uint32_t o[kOS];
     if (ld_ok) {
       tc_fence_after();
-      if constexpr (kOS == 32) tmem_ld32(o_col, o);
-      else tmem_ld16(o_col, o);
+#pragma unroll
+      for (int i = 0; i < kOS / 32; ++i) tmem_ld32(o_col + 32 * i, o + 32 * i);
       tmem_wait_ld();
     }
     if (row_ok) {
