@@ -15,6 +15,8 @@
 // is already known; each iteration therefore loads exactly one new key row.
 #include <math.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "launch.h"
 
@@ -52,8 +54,11 @@ __host__ __device__ inline size_t score_smem_q_off(bool explicit_list, int L) {
   return o;
 }
 
-template <typename T, int D, bool QREG>
-__global__ void __launch_bounds__(1024) stage_score_kernel(StageScoreArgs a) {
+// NT_MAX / MIN_B: launch bounds.  Up to 32 query heads (256 threads) the kernel keeps
+// eight CTAs (64 warps) resident per SM: every octet waits on one dependent key row at
+// a time, so the number of tournaments in flight is what feeds HBM.
+template <typename T, int D, bool QREG, int NT_MAX, int MIN_B>
+__global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreArgs a) {
   constexpr int EPL = D / 8;
   extern __shared__ __align__(16) unsigned char smem[];
   float *s_rho = reinterpret_cast<float *>(smem);
@@ -85,22 +90,38 @@ __global__ void __launch_bounds__(1024) stage_score_kernel(StageScoreArgs a) {
   if (h < a.H_q) {
     const int g = h / G;
     const unsigned omask = 0xffu << (threadIdx.x & 24);
-    float qv[QREG ? EPL : 1];
-    if (QREG) load_row<T, EPL>(q + static_cast<size_t>(h) * D + sub * EPL, qv);
+    constexpr int NV = EPL * static_cast<int>(sizeof(T)) / 16;   // 16-byte loads per lane
+    // the query slice stays in its storage format too (bf16 pairs or fp32)
+    uint4 qraw[QREG ? NV : 1];
+    if (QREG) {
+      const uint4 *qp = reinterpret_cast<const uint4 *>(q + static_cast<size_t>(h) * D + sub * EPL);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) qraw[i] = __ldg(qp + i);
+    }
     const T *kb = static_cast<const T *>(a.k) + static_cast<size_t>(b) * a.T_max * a.H_kv * D +
                   static_cast<size_t>(g) * D + sub * EPL;
     const size_t row_stride = static_cast<size_t>(a.H_kv) * D;
     const int T_q = QREG ? 1 : a.T_q;
     auto pos_of = [&](int x) -> int { return ir.in ? s_pos[x] : ir.start + base + x; };
     auto score = [&](int x) -> float {
-      float kf[EPL];
-      load_row<T, EPL>(kb + static_cast<size_t>(pos_of(x)) * row_stride, kf);
+      // keep the row as raw 16-byte words and widen while multiplying (fewer registers)
+      uint4 raw[NV];
+      const uint4 *kp = reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(pos_of(x)) * row_stride);
+#pragma unroll
+      for (int i = 0; i < NV; ++i) raw[i] = __ldg(kp + i);
       float best = -INFINITY;
       for (int t = 0; t < T_q; ++t) {
-        const float *qq = QREG ? qv : s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
+        const float *qq = s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
         float d = 0.f;
+        constexpr int per = Store<T>::kPer16;
 #pragma unroll
-        for (int e = 0; e < EPL; ++e) d = fmaf(qq[e], kf[e], d);
+        for (int i = 0; i < NV; ++i) {
+          float kf[per], qf[per];
+          unpack16(raw[i], kf, T());
+          if (QREG) unpack16(qraw[i], qf, T());
+#pragma unroll
+          for (int e = 0; e < per; ++e) d = fmaf(QREG ? qf[e] : qq[i * per + e], kf[e], d);
+        }
         d += __shfl_xor_sync(omask, d, 4);
         d += __shfl_xor_sync(omask, d, 2);
         d += __shfl_xor_sync(omask, d, 1);
@@ -201,6 +222,330 @@ __global__ void __launch_bounds__(kTopkThreads) stage_topk_kernel(StageTopkArgs 
   }
 }
 
+// Register-resident top-K for up to kFastNT * kFastNPT chunks.  Thread t owns the
+// kFastNPT consecutive chunks starting at t * kFastNPT, so one block-wide scan of
+// per-thread counts ranks the kept chunks in index order.
+// Selection: the ordered keys are spread over kFastNB buckets by a map that never
+// decreases with the key (equal keys share a bucket; a higher bucket holds only
+// larger keys).  One histogram and one scan find the bucket holding the K-th largest
+// key; only that bucket's members (usually a handful) are ranked exactly, by key and
+// then by chunk index.  When more than kFastCand keys share the boundary bucket (many
+// equal scores), an 8-bit radix select over the resident keys decides instead.
+constexpr int kFastNT = 1024;
+constexpr int kFastNPT = 16;
+constexpr int kFastNB = 4096;
+constexpr int kFastCand = 1024;
+
+// inclusive block scan of one value per thread (thread order); all threads call it
+__device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *s_w, uint32_t *total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  uint32_t incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const uint32_t u = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += u;
+  }
+  if (lane == 31) s_w[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    const uint32_t x = lane < kFastNT / 32 ? s_w[lane] : 0u;
+    uint32_t w = x;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const uint32_t u = __shfl_up_sync(kFull, w, o);
+      if (lane >= o) w += u;
+    }
+    if (lane < kFastNT / 32) s_w[lane] = w - x;
+    if (lane == 31) s_w[kFastNT / 32] = w;
+  }
+  __syncthreads();
+  const uint32_t r = s_w[warp] + incl;
+  *total = s_w[kFastNT / 32];
+  __syncthreads();   // s_w may be reused right away
+  return r;
+}
+
+// POW2: 16-byte access to the score row and the token lists (see the host side).
+// NPT: chunks per thread, the smallest power of two with kFastNT * NPT >= max_chunks,
+// so that no thread walks empty slots.
+template <bool POW2, int NPT>
+__global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs a) {
+  constexpr int NT = kFastNT, NB = kFastNB;
+  extern __shared__ int s_chunk_of_rank[];   // [K]
+  __shared__ uint32_t s_hist[NB];
+  __shared__ uint32_t s_ckey[kFastCand];
+  __shared__ int s_cidx[kFastCand];
+  __shared__ uint32_t s_keep[(NT * NPT + 31) / 32];   // kept bits of boundary-bucket chunks
+  __shared__ uint32_t s_w[NT / 32 + 1];
+  __shared__ uint32_t s_misc[8];   // 0 min, 1 max, 2 boundary bucket, 3 count above, 4 candidates
+  __shared__ uint32_t s_hist8[256];
+  __shared__ uint32_t s_res[2];
+  const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int i0 = tid * NPT;
+  // the row's scores come in while the candidate range is read (slots past the row's
+  // chunk count are ignored below)
+  const float *sc = a.score + static_cast<size_t>(b) * a.max_chunks;
+  float sv[NPT];
+  if (POW2 && NPT % 4 == 0 && i0 + NPT <= a.max_chunks) {
+#pragma unroll
+    for (int k = 0; k < NPT; k += 4) {
+      const float4 f = __ldg(reinterpret_cast<const float4 *>(sc + i0 + k));
+      sv[k] = f.x;
+      sv[k + 1] = f.y;
+      sv[k + 2] = f.z;
+      sv[k + 3] = f.w;
+    }
+  } else {
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) sv[k] = i0 + k < a.max_chunks ? __ldg(sc + i0 + k) : 0.f;
+  }
+  const InputRange ir = stage_input(a.kv_len, b, a.T_max, a.n_sink, a.n_stream, a.in_idx,
+                                    a.in_cnt, a.in_stride);
+  const int L = a.L;
+  const int n_chunk = min((ir.n_in + L - 1) / L, a.max_chunks);
+  const bool keep_all = n_chunk <= a.K;
+  uint32_t key[NPT];
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) key[k] = (i0 + k < n_chunk) ? ordered_key(sv[k]) : 0u;
+  uint32_t kept_bits = 0u;   // bit k: chunk i0 + k is kept
+  if (keep_all) {
+#pragma unroll
+    for (int k = 0; k < NPT; ++k)
+      if (i0 + k < n_chunk) kept_bits |= 1u << k;
+  } else {
+    // key range of the row
+    uint32_t mn = 0xffffffffu, mx = 0u;
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+      if (i0 + k < n_chunk) {
+        mn = min(mn, key[k]);
+        mx = max(mx, key[k]);
+      }
+    }
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    for (int i = tid; i < NB; i += NT) s_hist[i] = 0u;
+    for (int i = tid; i < (NT * NPT + 31) / 32; i += NT) s_keep[i] = 0u;
+    if (lane == 0) {
+      s_hist8[warp] = mn;          // scratch for the block reduction
+      s_hist8[32 + warp] = mx;
+    }
+    if (tid == 0) s_misc[4] = 0u;
+    __syncthreads();
+    if (warp == 0) {
+      const uint32_t m0 = __reduce_min_sync(kFull, s_hist8[lane]);
+      const uint32_t m1 = __reduce_max_sync(kFull, s_hist8[32 + lane]);
+      if (lane == 0) {
+        s_misc[0] = m0;
+        s_misc[1] = m1;
+      }
+    }
+    __syncthreads();
+    const uint32_t kmin = s_misc[0];
+    const float bscale = static_cast<float>(NB) / (static_cast<float>(s_misc[1] - kmin) + 1.0f);
+    // never decreasing in the key: a uint32 -> float conversion keeps order (ties at
+    // worst), as do the positive scaling and the truncation
+    auto bucket = [&](uint32_t u) {
+      return min(NB - 1, static_cast<int>(static_cast<float>(u - kmin) * bscale));
+    };
+#pragma unroll
+    for (int k = 0; k < NPT; ++k)
+      if (i0 + k < n_chunk) atomicAdd(&s_hist[bucket(key[k])], 1u);
+    __syncthreads();
+    // thread t holds buckets NB-1-4t .. NB-4-4t; counts from the top bucket down
+    uint32_t c4[4], sum4 = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      c4[j] = s_hist[NB - 1 - 4 * tid - j];
+      sum4 += c4[j];
+    }
+    uint32_t total;
+    const uint32_t incl = block_incl_scan(sum4, s_w, &total);
+    const uint32_t K = static_cast<uint32_t>(a.K);
+    if (incl - sum4 < K && K <= incl) {
+      uint32_t run = incl - sum4;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        if (run + c4[j] >= K) {
+          s_misc[2] = static_cast<uint32_t>(NB - 1 - 4 * tid - j);
+          s_misc[3] = run;
+          break;
+        }
+        run += c4[j];
+      }
+    }
+    __syncthreads();
+    const int bstar = static_cast<int>(s_misc[2]);
+    const uint32_t above = s_misc[3];
+    // the boundary bucket's members
+#pragma unroll
+    for (int k = 0; k < NPT; ++k) {
+      const bool valid = i0 + k < n_chunk;
+      const int bk = valid ? bucket(key[k]) : -1;
+      if (bk > bstar) kept_bits |= 1u << k;
+      // one slot claim per warp and key position
+      const unsigned members = __ballot_sync(kFull, bk == bstar);
+      if (members) {
+        uint32_t base = 0;
+        if (lane == __ffs(members) - 1) base = atomicAdd(&s_misc[4], static_cast<uint32_t>(__popc(members)));
+        base = __shfl_sync(kFull, base, __ffs(members) - 1);
+        if (bk == bstar) {
+          const uint32_t slot = base + __popc(members & ((1u << lane) - 1u));
+          if (slot < static_cast<uint32_t>(kFastCand)) {
+            s_ckey[slot] = key[k];
+            s_cidx[slot] = i0 + k;
+          }
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t m = s_misc[4];
+    if (m <= static_cast<uint32_t>(kFastCand)) {
+      // exact ranks inside the bucket: larger key first, then smaller chunk index
+      const uint32_t need = K - above;   // 1 <= need <= m
+      for (uint32_t j = tid; j < m; j += NT) {
+        const uint32_t kj = s_ckey[j];
+        const int ij = s_cidx[j];
+        uint32_t rank = 0;
+        for (uint32_t i = 0; i < m; ++i) {
+          const uint32_t ki = s_ckey[i];
+          rank += (ki > kj || (ki == kj && s_cidx[i] < ij)) ? 1u : 0u;
+        }
+        if (rank < need) atomicOr(&s_keep[ij >> 5], 1u << (ij & 31));
+      }
+      __syncthreads();
+#pragma unroll
+      for (int k = 0; k < NPT; ++k) {
+        const int i = i0 + k;
+        if (i < n_chunk && bucket(key[k]) == bstar && ((s_keep[i >> 5] >> (i & 31)) & 1u))
+          kept_bits |= 1u << k;
+      }
+    } else {
+      // many equal or nearly equal keys: radix select over the resident keys for the
+      // K-th largest key `thr` and the number `k_eq` of its copies in the top K, then
+      // keep the first k_eq copies in index order
+      uint32_t prefix = 0u, mask = 0u, k_rem = K;
+      for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        for (int i = tid; i < 256; i += NT) s_hist8[i] = 0u;
+        __syncthreads();
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) {
+          const bool ok = i0 + k < n_chunk && (key[k] & mask) == prefix;
+          const uint32_t bin = ok ? ((key[k] >> shift) & 255u) : 256u;
+          const unsigned peers = __match_any_sync(kFull, bin);
+          if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist8[bin], static_cast<uint32_t>(__popc(peers)));
+        }
+        __syncthreads();
+        if (warp == 0) {
+          const int top = 255 - lane * 8;
+          uint32_t c[8], sum = 0;
+#pragma unroll
+          for (int t = 0; t < 8; ++t) {
+            c[t] = s_hist8[top - t];
+            sum += c[t];
+          }
+          uint32_t inc = sum;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t v = __shfl_up_sync(kFull, inc, o);
+            if (lane >= o) inc += v;
+          }
+          const uint32_t exc = inc - sum;
+          if (exc < k_rem && k_rem <= inc) {
+            uint32_t run = exc;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              if (run + c[t] >= k_rem) {
+                s_res[0] = static_cast<uint32_t>(top - t);
+                s_res[1] = run;
+                break;
+              }
+              run += c[t];
+            }
+          }
+        }
+        __syncthreads();
+        prefix |= s_res[0] << shift;
+        mask |= 255u << shift;
+        k_rem -= s_res[1];
+        __syncthreads();
+      }
+      const uint32_t thr = prefix, k_eq = k_rem;
+      uint32_t eq = 0;
+#pragma unroll
+      for (int k = 0; k < NPT; ++k) eq += (i0 + k < n_chunk && key[k] == thr) ? 1u : 0u;
+      uint32_t tot_eq;
+      uint32_t eq_b = block_incl_scan(eq, s_w, &tot_eq) - eq;
+      kept_bits = 0u;
+#pragma unroll
+      for (int k = 0; k < NPT; ++k) {
+        if (i0 + k < n_chunk) {
+          if (key[k] > thr) kept_bits |= 1u << k;
+          if (key[k] == thr) {
+            if (eq_b < k_eq) kept_bits |= 1u << k;
+            ++eq_b;
+          }
+        }
+      }
+    }
+  }
+  // ranks of the kept chunks in index order
+  const uint32_t nk = static_cast<uint32_t>(__popc(kept_bits));
+  uint32_t tot_kept;
+  uint32_t r = block_incl_scan(nk, s_w, &tot_kept) - nk;
+#pragma unroll
+  for (int k = 0; k < NPT; ++k) {
+    if ((kept_bits >> k) & 1u) {
+      if (r < static_cast<uint32_t>(a.K)) s_chunk_of_rank[r] = i0 + k;
+      ++r;
+    }
+  }
+  __syncthreads();
+  const int n_kept = min(static_cast<int>(tot_kept), max(a.K, 0));
+  int count = n_kept * L;
+  // only the last chunk of the list can be short; kept, it has the highest rank
+  if (n_kept > 0 && s_chunk_of_rank[n_kept - 1] == n_chunk - 1) count -= n_chunk * L - ir.n_in;
+  int32_t *out = a.out_idx + static_cast<size_t>(b) * a.out_stride;
+  int32_t *dbg = a.dbg_idx ? a.dbg_idx + static_cast<size_t>(b) * a.out_stride : nullptr;
+  if (POW2 && (L & 3) == 0 && (a.out_stride & 3) == 0) {
+    // four consecutive entries share a chunk: 16-byte loads and stores
+    const int lg = __ffs(L) - 1;
+    for (int e = 4 * tid; e < a.out_stride; e += 4 * NT) {
+      int4 val = make_int4(-1, -1, -1, -1);
+      if (e < count) {
+        const int rr = e >> lg, x = e & (L - 1);
+        const int src = (s_chunk_of_rank[rr] << lg) + x;
+        if (ir.in) {
+          val = *reinterpret_cast<const int4 *>(ir.in + src);
+        } else {
+          val = make_int4(ir.start + src, ir.start + src + 1, ir.start + src + 2, ir.start + src + 3);
+        }
+        if (e + 1 >= count) val.y = -1;
+        if (e + 2 >= count) val.z = -1;
+        if (e + 3 >= count) val.w = -1;
+      }
+      *reinterpret_cast<int4 *>(out + e) = val;
+      if (dbg) *reinterpret_cast<int4 *>(dbg + e) = val;
+    }
+  } else {
+    for (int e = tid; e < a.out_stride; e += NT) {
+      int val = -1;
+      if (e < count) {
+        const int rr = e / L, x = e - rr * L;
+        const int src = s_chunk_of_rank[rr] * L + x;
+        val = ir.in ? ir.in[src] : ir.start + src;
+      }
+      out[e] = val;
+      if (dbg) dbg[e] = val;
+    }
+  }
+  if (tid == 0) {
+    a.out_cnt[b] = count;
+    if (a.dbg_cnt) a.dbg_cnt[b] = count;
+  }
+}
+
 template <typename T, int D>
 cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
   const bool explicit_list = a.in_idx != nullptr;
@@ -210,15 +555,14 @@ cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
   const int threads = ((8 * a.H_q + 31) / 32) * 32;
   dim3 grid(a.max_chunks, a.B);
   if (a.max_chunks == 0) return cudaSuccess;
-  if (qreg) {
-    auto kern = stage_score_kernel<T, D, true>;
+  auto go = [&](auto kern) {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     kern<<<grid, threads, smem, s>>>(a);
-  } else {
-    auto kern = stage_score_kernel<T, D, false>;
-    if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, threads, smem, s>>>(a);
-  }
+  };
+  // fp32 rows need twice the registers: six CTAs per SM there
+  if (qreg && threads <= 256) go(stage_score_kernel<T, D, true, 256, sizeof(T) == 2 ? 8 : 6>);
+  else if (qreg) go(stage_score_kernel<T, D, true, 1024, 1>);
+  else go(stage_score_kernel<T, D, false, 1024, 1>);
   return cudaGetLastError();
 }
 
@@ -233,9 +577,35 @@ cudaError_t launch_stage_score(const StageScoreArgs &a, cudaStream_t s) {
 
 cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(a.K) * sizeof(int);
-  if (smem > 48 * 1024)
-    cudaFuncSetAttribute(stage_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  stage_topk_kernel<<<a.B, kTopkThreads, smem, s>>>(a);
+  // static shared memory: about 28 KB in the register-resident kernel, 1 KB otherwise
+  auto go = [&](auto kern, int threads, size_t static_bytes) {
+    if (smem + static_bytes > 48 * 1024)
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    kern<<<a.B, threads, smem, s>>>(a);
+  };
+  // 16-byte list access needs 16-byte aligned rows of the explicit input list, and rows
+  // holding whole chunks (the last chunk's 16-byte groups then stay inside the row)
+  const bool pow2 = (a.L & (a.L - 1)) == 0 && (reinterpret_cast<uintptr_t>(a.score) & 15) == 0 &&
+                    (a.max_chunks & 3) == 0 &&
+                    (a.in_idx == nullptr ||
+                     ((reinterpret_cast<uintptr_t>(a.in_idx) & 15) == 0 && (a.in_stride & 3) == 0 &&
+                      a.in_stride % a.L == 0)) &&
+                    (reinterpret_cast<uintptr_t>(a.out_idx) & 15) == 0 &&
+                    (a.dbg_idx == nullptr || (reinterpret_cast<uintptr_t>(a.dbg_idx) & 15) == 0);
+  if (a.max_chunks <= kFastNT * kFastNPT) {
+    auto pick = [&](auto pw) {
+      constexpr bool P = decltype(pw)::value;
+      if (a.max_chunks <= kFastNT) go(stage_topk_fast_kernel<P, 1>, kFastNT, 28 * 1024);
+      else if (a.max_chunks <= 2 * kFastNT) go(stage_topk_fast_kernel<P, 2>, kFastNT, 28 * 1024);
+      else if (a.max_chunks <= 4 * kFastNT) go(stage_topk_fast_kernel<P, 4>, kFastNT, 28 * 1024);
+      else if (a.max_chunks <= 8 * kFastNT) go(stage_topk_fast_kernel<P, 8>, kFastNT, 28 * 1024);
+      else go(stage_topk_fast_kernel<P, 16>, kFastNT, 28 * 1024);
+    };
+    if (pow2) pick(std::true_type{});
+    else pick(std::false_type{});
+  } else {
+    go(stage_topk_kernel, kTopkThreads, 2 * 1024);
+  }
   return cudaGetLastError();
 }
 

@@ -94,6 +94,36 @@ def test_non_power_of_two_chunks():
     _check_case(c)
 
 
+def test_more_chunks_than_register_topk():
+    """Stage 0 with 17,971 chunks: past the register-resident top-K (16,384 chunks), so
+    the selection takes the general kernel; stage 1 takes the register one."""
+    c = decode_case("many", B=1, T=36000, T_q=1, H_q=2, H_kv=1, D=64, dtype="bf16",
+                    chunk=(2, 1), keep=(4096, 1024), n_sink=7, n_stream=50, seed=36,
+                    plant="uniform", n_plant=8)
+    _check_case(c)
+
+
+def test_topk_ties_in_boundary_bucket():
+    """Keys repeat with period 61, so chunk scores take few distinct values and the
+    bucket holding the K-th score holds several equal scores: ties go to the smaller
+    chunk index."""
+    c = decode_case("ties", B=1, T=12000, T_q=1, H_q=4, H_kv=1, D=64, dtype="bf16",
+                    chunk=(16, 4), keep=(2048, 512), n_sink=4, n_stream=32, seed=37,
+                    plant="none")
+    c.k[0, 61:] = c.k[0, np.arange(61, 12000) % 61]
+    _check_case(c)
+
+
+def test_topk_all_scores_equal():
+    """A zero query makes every chunk score 0: more equal scores than the exact-rank
+    path takes, so the selection falls back to the radix select."""
+    c = decode_case("zeroq", B=1, T=20000, T_q=1, H_q=4, H_kv=2, D=64, dtype="bf16",
+                    chunk=(8, 2), keep=(4096, 1024), n_sink=4, n_stream=32, seed=38,
+                    plant="none")
+    c.q[:] = 0
+    _check_case(c)
+
+
 def test_dense_keep_all_matches_sdpa():
     c = decode_case("dense", B=2, T=1500, T_q=1, H_q=8, H_kv=2, D=128, dtype="bf16",
                     chunk=(64, 16), keep=(1 << 14, 1 << 14), n_sink=4, n_stream=16, seed=35,
