@@ -425,7 +425,8 @@ def main():
     attn_bytes = attended * dec.H_kv * dec.D * elem * 2 + 2 * dec.T_q * dec.H_q * dec.D * elem
     step_bytes = sum(r * dec.D * elem for r in stage_rows) + attn_bytes
     dec_kernel_bytes = {f"hip_stage_score_s{i}": b for i, b in enumerate(stage_bytes)}
-    dec_kernel_bytes["decode_splitk"] = attn_bytes
+    for name in ("decode_splitk", "decode_cluster_mma"):   # whichever attention kernel ran
+        dec_kernel_bytes[name] = attn_bytes
     for name, b in dec_kernel_bytes.items():
         if name in kern:
             kern[name]["algorithmic_bytes"] = b

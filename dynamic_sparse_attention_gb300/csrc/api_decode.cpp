@@ -210,10 +210,11 @@ int sparse_attn_decode_workspace(const dsa_decode_shape *shape, int max_sel, int
   if (!bytes) return fail(DSA_ERR_ALIGNMENT, "bytes is NULL");
   const long a_max = attended_max(shape, max_sel, n_sink, n_stream);
   if (a_max > 0x7fffffffL) return fail(DSA_ERR_INVALID_ARG, "attended set too large");
-  int n_split, kps;
-  decode_plan(shape->B, shape->H_kv, static_cast<int>(a_max), &n_split, &kps);
+  const int R = (shape->H_q / shape->H_kv) * shape->T_q;
+  const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
+  const size_t nf = decode_ws_floats(plan, shape->B, shape->T_q, shape->H_q, shape->D);
   Carve cv(nullptr);
-  cv.take<float>(static_cast<size_t>(shape->B) * n_split * shape->T_q * shape->H_q * (shape->D + 2));
+  if (nf) cv.take<float>(nf);
   *bytes = cv.bytes();
   return DSA_OK;
 }
@@ -238,13 +239,12 @@ int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_
   if (lse && !aligned(lse, 4)) return fail(DSA_ERR_ALIGNMENT, "lse must be 4-byte aligned");
   const long a_max = attended_max(shape, max_sel, n_sink, n_stream);
   if (a_max > 0x7fffffffL) return fail(DSA_ERR_INVALID_ARG, "attended set too large");
-  int n_split, kps;
-  decode_plan(shape->B, shape->H_kv, static_cast<int>(a_max), &n_split, &kps);
-  if (n_split > 65535) return fail(DSA_ERR_INVALID_ARG, "too many splits (%d)", n_split);
+  const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
+  if (plan.n_split > 65535) return fail(DSA_ERR_INVALID_ARG, "too many splits (%d)", plan.n_split);
+  const size_t nf = decode_ws_floats(plan, shape->B, shape->T_q, shape->H_q, shape->D);
   Carve cv(ws);
-  float *part =
-      cv.take<float>(static_cast<size_t>(shape->B) * n_split * shape->T_q * shape->H_q * (shape->D + 2));
-  if (ws_bytes < cv.bytes() || !aligned(ws, 16))
+  float *part = nf ? cv.take<float>(nf) : nullptr;
+  if (ws_bytes < cv.bytes() || (nf && !aligned(ws, 16)))
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu",
                 cv.bytes(), ws_bytes);
   DecodeArgs a{};
@@ -265,8 +265,9 @@ int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_
   a.H_kv = shape->H_kv;
   a.D = shape->D;
   a.dtype = shape->dtype;
-  a.n_split = n_split;
-  a.keys_per_split = kps;
+  a.n_split = plan.n_split;
+  a.keys_per_split = plan.keys_per_split;
+  a.cluster = plan.cluster;
   a.part = part;
   a.out = out;
   a.lse = lse;

@@ -10,10 +10,14 @@
 // "Chunk-Level Attention Scoring Engine" gives the same union-of-tiers softmax with
 // a 1/sqrt(d_k) scale.
 //
-// Layout: grid = (split, KV head g, batch b).  The CTA serves all G query heads of
-// KV head g and all T_q query rows at once, so each selected K/V row is gathered
-// from HBM exactly once per split: 64-key tiles are staged into shared memory with
-// 16-byte cp.async gathers (a token's row for head g is contiguous, 2*D bytes).
+// Layout: the CTA serves all G query heads of KV head g and all T_q query rows at
+// once, so each selected K/V row is gathered from HBM exactly once: 64-key tiles are
+// staged into shared memory with 16-byte cp.async gathers (a token's row for head g
+// is contiguous, 2*D bytes).
+// This file holds the split path, for fp32 inputs and for more than 16 query rows
+// per KV head: grid = (split, g, b) writes partials, a second kernel merges them.
+// bf16 with at most 16 rows per KV head takes the tensor-core cluster kernel of
+// decode_mma.cu.
 #include <math.h>
 
 #include "common.cuh"
@@ -268,6 +272,7 @@ template <typename T, int D>
 cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t s) {
   const int R = (a.H_q / a.H_kv) * a.T_q;
   const int need = (R * D + kNT - 1) / kNT;
+
   if (need <= 1) return launch_decode_t<T, D, 1>(a, s);
   if (need <= 2) return launch_decode_t<T, D, 2>(a, s);
   if (need <= 4) return launch_decode_t<T, D, 4>(a, s);
@@ -278,17 +283,34 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t s) {
 
 }  // namespace
 
-void decode_plan(int B, int H_kv, int a_max, int *n_split, int *keys_per_split) {
-  // aim for about two CTAs per SM of a 152-SM part; splits are whole 64-key tiles
+DecodePlan decode_plan(int B, int H_kv, int R, int D, int dtype, int a_max) {
+  DecodePlan p{};
+  if (dtype == 0 && R <= 16) {
+    // tensor-core cluster path: up to 16 CTAs per (b, g), whole 16-key sub-tiles each
+    constexpr int kSub = 16;
+    const int subs = a_max > 0 ? (a_max + kSub - 1) / kSub : 1;
+    p.cluster = true;
+    p.n_split = subs < 16 ? subs : 16;
+    p.keys_per_split = ((subs + p.n_split - 1) / p.n_split) * kSub;
+    return p;
+  }
+  // split path: about two CTAs per SM of a 152-SM part
+  p.cluster = false;
   const int target = (304 + B * H_kv - 1) / (B * H_kv);
   int kps = (a_max + target - 1) / (target > 0 ? target : 1);
   kps = ((kps + kTK - 1) / kTK) * kTK;
   if (kps < kTK) kps = kTK;
-  *keys_per_split = kps;
-  *n_split = a_max > 0 ? (a_max + kps - 1) / kps : 1;
+  p.keys_per_split = kps;
+  p.n_split = a_max > 0 ? (a_max + kps - 1) / kps : 1;
+  return p;
+}
+
+size_t decode_ws_floats(const DecodePlan &p, int B, int T_q, int H_q, int D) {
+  return p.cluster ? 0 : static_cast<size_t>(B) * p.n_split * T_q * H_q * (D + 2);
 }
 
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s) {
+  if (a.cluster) return launch_decode_mma(a, s);
   if (a.dtype == 0) return a.D == 128 ? launch_decode_d<uint16_t, 128>(a, s) : launch_decode_d<uint16_t, 64>(a, s);
   return a.D == 128 ? launch_decode_d<float, 128>(a, s) : launch_decode_d<float, 64>(a, s);
 }

@@ -1,0 +1,408 @@
+// Sparse GQA decode on warp-level tensor cores, one thread-block cluster per
+// (batch row b, KV head g).
+//
+// Source: "InfiniteHiP: Extending Language Model Context Up to 3 Million Tokens on a
+// Single GPU" (paper-graph-ui summary), section 3.4 "Block Sparse Attention
+// Implementation" (decoding: split the keys across thread blocks, partial softmax,
+// final reduction) and "Formal Background" (softmax attention).
+//
+// Decode is bound by the latency of gathering a few thousand scattered K/V rows, not
+// by arithmetic.  The design therefore puts every gather in flight early and keeps
+// the per-key work on tensor cores:
+//  * the cluster's CTAs (up to 16) split the attended keys of (b, g); inside a CTA
+//    each warp owns every fourth 16-key sub-tile, gathers it (16-byte cp.async, a
+//    token's row for head g is 2*D contiguous bytes) into its own shared-memory ring
+//    with kNBuf sub-tiles in flight, and keeps its own online softmax; the key
+//    positions of a CTA's range are read in one round (the selected slots are read
+//    before the row's sink count is known, on the assumption that it is full);
+//  * S = Q K^T and O += P V are mma.sync m16n8k16 (bf16 in, fp32 accumulate): the
+//    G*T_q query rows (at most 16) of the KV head are the M = 16 rows, keys and head
+//    dimensions the N and K sides; P goes from the S accumulators straight into the A
+//    operand of the P V product;
+//  * the running max is exact (the row's largest probability is exactly 1) and the
+//    row sum adds the same bf16-rounded probabilities that enter P V;
+//  * at the end the four warps of a CTA merge in shared memory and the CTAs of the
+//    cluster merge through distributed shared memory (log-sum-exp weights); nothing
+//    goes through HBM but the K/V rows, the query and the output.
+#include <cooperative_groups.h>
+#include <math.h>
+
+#include "common.cuh"
+#include "launch.h"
+#include "mma_sync.cuh"
+#include "profile.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kST = 16;      // keys per warp sub-tile
+constexpr int kNBuf = 3;     // sub-tiles in flight per warp (two CTAs fit an SM)
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// Shared rows are D bf16 with the 16-byte pieces of key row k stored at piece index
+// c ^ (k & 7): the eight rows an ldmatrix reads at one piece index hit eight
+// different bank groups.
+template <int D>
+struct MmaSmem {
+  static constexpr int kRow = D;                // bf16 per shared row
+  static constexpr int kSlot = 2 * kST * kRow;  // K rows then V rows of one sub-tile
+  static size_t bytes(int kps, int R) {
+    size_t o = static_cast<size_t>(kWarps) * kNBuf * kSlot * 2;   // the warps' rings
+    o += static_cast<size_t>(kps) * 4;                             // key positions
+    o += static_cast<size_t>(kWarps + 1) * R * (D + 2) * 4;        // warp and CTA partials
+    return o;
+  }
+};
+
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem_dst)),
+               "l"(gmem_src));
+}
+
+// element offset of piece c (8 bf16) of key row k in a swizzled tile
+template <int D>
+__device__ __forceinline__ int sw_off(int k, int c) {
+  return k * D + ((c ^ (k & 7)) << 3);
+}
+
+__device__ __forceinline__ float bf16r(float x) {   // x rounded to bf16 (nearest even)
+  return __uint_as_float(static_cast<uint32_t>(f32_to_bf16(x)) << 16);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
+  namespace cg = cooperative_groups;
+  using SM = MmaSmem<D>;
+  constexpr int KS = D / 16;   // k-steps of Q K^T
+  constexpr int NT = D / 8;    // n-tiles of P V
+  constexpr int CH = D / 8;    // 16-byte pieces per K or V row
+  extern __shared__ __align__(16) unsigned char smem[];
+  const int G = a.H_q / a.H_kv;
+  const int R = G * a.T_q;     // <= 16
+  uint16_t *ring = reinterpret_cast<uint16_t *>(smem);
+  int *s_pos = reinterpret_cast<int *>(ring + kWarps * kNBuf * SM::kSlot);
+  float *s_part = reinterpret_cast<float *>(s_pos + a.keys_per_split);   // [kWarps + 1][R][D + 2]
+
+  cg::cluster_group cluster = cg::this_cluster();
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int C = static_cast<int>(cluster.num_blocks());
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int gq = lane >> 2, tq = lane & 3;
+  const int32_t *sel = a.sel_idx + static_cast<size_t>(b) * a.max_sel;
+  const int k_begin = rank * a.keys_per_split;
+  // the selected positions this range would hold if every sink slot were filled, read
+  // together with the row's length and count (one round of loads instead of two)
+  constexpr int kSpec = 4;
+  int spec[kSpec];
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int i = tid + u * kThreads;
+    const int xs = k_begin + i - a.n_sink;   // selected slot if n_s == n_sink
+    spec[u] = (i < a.keys_per_split && xs >= 0 && xs < a.max_sel) ? __ldg(sel + xs) : -1;
+  }
+  const int Tb = min(max(a.kv_len[b], 0), a.T_max);
+  const int n_s = min(a.n_sink, Tb);
+  const int cnt = min(max(a.sel_cnt[b], 0), a.max_sel);
+  const int w0 = max(a.n_sink, Tb - a.n_stream);
+  const int n_w = max(0, Tb - w0);
+  const int a_len = n_s + cnt + n_w;
+  const int k_end = min(a_len, k_begin + a.keys_per_split);
+  const int n_sub = k_end > k_begin ? (k_end - k_begin + kST - 1) / kST : 0;
+  const uint16_t *q = static_cast<const uint16_t *>(a.q);
+  const uint16_t *kbase = static_cast<const uint16_t *>(a.k) +
+                          static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D;
+  const uint16_t *vbase = static_cast<const uint16_t *>(a.v) +
+                          static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D;
+  const size_t row_stride = static_cast<size_t>(a.H_kv) * D;
+  const float sl2 = a.scale * kLog2e;
+
+  // every key position of this CTA's range (-1: none)
+  auto position = [&](int i, int speculated) {
+    const int x = k_begin + i;
+    int pos = -1;
+    if (x < k_end) {
+      if (x < n_s) pos = x;
+      else if (x < n_s + cnt) pos = n_s == a.n_sink ? speculated : sel[x - n_s];
+      else pos = w0 + (x - n_s - cnt);
+      if (pos < 0 || pos >= Tb) pos = -1;   // never read outside the row's context
+    }
+    return pos;
+  };
+#pragma unroll
+  for (int u = 0; u < kSpec; ++u) {
+    const int i = tid + u * kThreads;
+    if (i < a.keys_per_split) s_pos[i] = position(i, spec[u]);
+  }
+  for (int i = tid + kSpec * kThreads; i < a.keys_per_split; i += kThreads) {
+    const int xs = k_begin + i - a.n_sink;
+    s_pos[i] = position(i, xs >= 0 && xs < a.max_sel ? sel[xs] : -1);
+  }
+  // the query rows as A fragments (row r = t * G + j of head g * G + j; rows >= R zero)
+  uint32_t qa[KS][4];
+  {
+    auto qpair = [&](int r, int d) -> uint32_t {
+      if (r >= R) return 0u;
+      const int t = r / G, h = g * G + (r - t * G);
+      return *reinterpret_cast<const uint32_t *>(q + ((static_cast<size_t>(b) * a.T_q + t) * a.H_q + h) * D + d);
+    };
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = qpair(gq, ks * 16 + 2 * tq);
+      qa[ks][1] = qpair(gq + 8, ks * 16 + 2 * tq);
+      qa[ks][2] = qpair(gq, ks * 16 + 8 + 2 * tq);
+      qa[ks][3] = qpair(gq + 8, ks * 16 + 8 + 2 * tq);
+    }
+  }
+  __syncthreads();
+
+  uint16_t *wring = ring + warp * kNBuf * SM::kSlot;
+  // sub-tile j of the CTA range -> ring slot `slot` (one commit group per call)
+  auto issue = [&](int j, int slot) {
+    if (j < n_sub) {
+      uint16_t *sk = wring + slot * SM::kSlot;
+      uint16_t *sv = sk + kST * SM::kRow;
+      const int *pj = s_pos + j * kST;
+#pragma unroll
+      for (int e = lane; e < kST * CH; e += 32) {
+        const int key = e / CH, c = e - key * CH;
+        const int pos = pj[key];
+        uint16_t *dk = sk + sw_off<D>(key, c);
+        uint16_t *dv = sv + sw_off<D>(key, c);
+        if (pos >= 0) {
+          cp_async16(dk, kbase + static_cast<size_t>(pos) * row_stride + c * 8);
+          cp_async16(dv, vbase + static_cast<size_t>(pos) * row_stride + c * 8);
+        } else {
+          *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
+        }
+      }
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
+  };
+
+  float o[NT][4];
+#pragma unroll
+  for (int i = 0; i < NT; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows gq and gq + 8
+
+#pragma unroll
+  for (int s = 0; s < kNBuf; ++s) issue(warp + s * kWarps, s);
+  for (int it = 0, j = warp; j < n_sub; ++it, j += kWarps) {
+    const int slot = it % kNBuf;
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(kNBuf - 1) : "memory");
+    __syncwarp();
+    const uint16_t *sk = wring + slot * SM::kSlot;
+    const uint16_t *sv = sk + kST * SM::kRow;
+    // S = Q K^T: two n-tiles of 8 keys
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int mtx = lane >> 3, rr = lane & 7;
+      const int key = (mtx >> 1) * 8 + rr;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        uint32_t bk[4];
+        ldsm_x4(bk, sk + sw_off<D>(key, 2 * ks + (mtx & 1)));
+        mma_16816(s[0], qa[ks], bk[0], bk[1]);
+        mma_16816(s[1], qa[ks], bk[2], bk[3]);
+      }
+    }
+    // scale, mask keys without a position, exact running max per row
+    const int *pj = s_pos + j * kST;
+    float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int key = nt * 8 + 2 * tq + (e & 1);
+        const float v = pj[key] >= 0 ? s[nt][e] * sl2 : -INFINITY;
+        s[nt][e] = v;
+        if (e < 2) mx0 = fmaxf(mx0, v);
+        else mx1 = fmaxf(mx1, v);
+      }
+    }
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+    mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+    mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+    const float n0 = fmaxf(m0, mx0), n1 = fmaxf(m1, mx1);
+    const float al0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - n0);
+    const float al1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - n1);
+    m0 = n0;
+    m1 = n1;
+    // probabilities, rounded to bf16 once: the same values feed P V and the row sums
+    uint32_t pa[4];
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const float p0 = n0 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][0] - n0));
+      const float p1 = n0 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][1] - n0));
+      const float p2 = n1 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][2] - n1));
+      const float p3 = n1 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][3] - n1));
+      ps0 += p0 + p1;
+      ps1 += p2 + p3;
+      pa[2 * nt] = pack_bf16x2(p0, p1);       // a0 (n-tile 0) / a2 (n-tile 1): row gq
+      pa[2 * nt + 1] = pack_bf16x2(p2, p3);   // a1 / a3: row gq + 8
+    }
+    ps0 += __shfl_xor_sync(kFull, ps0, 1);
+    ps0 += __shfl_xor_sync(kFull, ps0, 2);
+    ps1 += __shfl_xor_sync(kFull, ps1, 1);
+    ps1 += __shfl_xor_sync(kFull, ps1, 2);
+    l0 = l0 * al0 + ps0;
+    l1 = l1 * al1 + ps1;
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      o[i][0] *= al0;
+      o[i][1] *= al0;
+      o[i][2] *= al1;
+      o[i][3] *= al1;
+    }
+    // O += P V: V rows (keys) are the K side, head dimensions the N side
+    {
+      const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
+      const int mtx = lane >> 3, rr = lane & 7;
+      const int key = (mtx & 1) * 8 + rr;
+#pragma unroll
+      for (int dp = 0; dp < D / 16; ++dp) {
+        uint32_t bv[4];
+        ldsm_x4_trans(bv, sv + sw_off<D>(key, 2 * dp + (mtx >> 1)));
+        mma_16816(o[2 * dp], pfrag, bv[0], bv[1]);
+        mma_16816(o[2 * dp + 1], pfrag, bv[2], bv[3]);
+      }
+    }
+    __syncwarp();
+    issue(j + kNBuf * kWarps, slot);
+  }
+  asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+
+  // this warp's partial for the rows it holds
+  {
+    float *wp = s_part + static_cast<size_t>(warp) * R * (D + 2);
+#pragma unroll
+    for (int i = 0; i < NT; ++i) {
+      const int d = i * 8 + 2 * tq;
+      if (gq < R) {
+        wp[gq * (D + 2) + d] = o[i][0];
+        wp[gq * (D + 2) + d + 1] = o[i][1];
+      }
+      if (gq + 8 < R) {
+        wp[(gq + 8) * (D + 2) + d] = o[i][2];
+        wp[(gq + 8) * (D + 2) + d + 1] = o[i][3];
+      }
+    }
+    if (tq == 0) {
+      if (gq < R) {
+        wp[gq * (D + 2) + D] = m0;
+        wp[gq * (D + 2) + D + 1] = l0;
+      }
+      if (gq + 8 < R) {
+        wp[(gq + 8) * (D + 2) + D] = m1;
+        wp[(gq + 8) * (D + 2) + D + 1] = l1;
+      }
+    }
+  }
+  __syncthreads();
+  // the CTA's partial from its four warps
+  float *cp = s_part + static_cast<size_t>(kWarps) * R * (D + 2);
+  for (int e = tid; e < R * (D + 1); e += kThreads) {
+    const int r = e / (D + 1), d = e - r * (D + 1);   // d == D: the row's (m, l)
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_part[(w * R + r) * (D + 2) + D]);
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) {
+      const float *wr = s_part + (w * R + r) * (D + 2);
+      const float wgt = (wr[D] == -INFINITY) ? 0.f : exp2f(wr[D] - M);
+      acc = fmaf(d < D ? wr[d] : wr[D + 1], wgt, acc);
+    }
+    if (d < D) {
+      cp[r * (D + 2) + d] = acc;
+    } else {
+      cp[r * (D + 2) + D] = M;
+      cp[r * (D + 2) + D + 1] = acc;
+    }
+  }
+  cluster.sync();
+  // merge across the cluster: the CTAs share the R*D outputs
+  const int E = R * D;
+  const int per = (E + C - 1) / C;
+  const int e_end = min(E, (rank + 1) * per);
+  for (int e = rank * per + tid; e < e_end; e += kThreads) {
+    const int r = e / D, d = e - r * D;
+    const float *pr = cp + r * (D + 2);
+    float M = -INFINITY;
+    for (int c = 0; c < C; ++c) M = fmaxf(M, *cluster.map_shared_rank(pr + D, c));
+    float Ls = 0.f, ov = 0.f;
+    if (M != -INFINITY) {
+      for (int c = 0; c < C; ++c) {
+        const float m = *cluster.map_shared_rank(pr + D, c);
+        if (m == -INFINITY) continue;
+        const float wgt = exp2f(m - M);
+        Ls = fmaf(*cluster.map_shared_rank(pr + D + 1, c), wgt, Ls);
+        ov = fmaf(*cluster.map_shared_rank(pr + d, c), wgt, ov);
+      }
+    }
+    const int t = r / G, h = g * G + (r - t * G);
+    const size_t row = (static_cast<size_t>(b) * a.T_q + t) * a.H_q + h;
+    static_cast<uint16_t *>(a.out)[row * D + d] = f32_to_bf16(Ls > 0.f ? ov / Ls : 0.f);
+    if (a.lse && d == 0) a.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+  }
+  cluster.sync();   // keep this CTA's shared memory until every reader is done
+}
+
+template <int D>
+cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
+  DecodeArgs a = a0;
+  const int R = (a.H_q / a.H_kv) * a.T_q;
+  const int keys = a.n_split * a.keys_per_split;
+  // shared memory sized for the larger range of the 8-CTA fallback below
+  const int kps8 = ((keys / 8 + kST - 1) / kST) * kST;
+  const size_t smem = MmaSmem<D>::bytes(kps8 > a.keys_per_split ? kps8 : a.keys_per_split, R);
+  auto kern = decode_mma_kernel<D>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  if (a.n_split > 8) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(a.n_split, a.H_kv, a.B);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = a.n_split;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // a device that cannot co-schedule 16 CTAs of this size gets clusters of 8
+  if (a.n_split > 8) {
+    int n_clusters = 0;
+    if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess || n_clusters < 1) {
+      (void)cudaGetLastError();
+      a.n_split = 8;
+      a.keys_per_split = kps8;
+      cfg.gridDim.x = 8;
+      attr[0].val.clusterDim.x = 8;
+    }
+  }
+  {
+    ProfScope ps("decode_cluster_mma", s);
+    e = cudaLaunchKernelEx(&cfg, kern, a);
+  }
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t s) {
+  return a.D == 128 ? launch_mma_d<128>(a, s) : launch_mma_d<64>(a, s);
+}
+
+}  // namespace dsa

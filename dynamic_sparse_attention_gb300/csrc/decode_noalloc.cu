@@ -83,8 +83,7 @@ int sparse_attn_decode_noalloc(const void *q, const void *k, const void *v,
   if ((st = static_scratch(&part))) return st;
   const long a_max = static_cast<long>(n_sink < shape->T_max ? n_sink : shape->T_max) + max_sel +
                      (n_stream < shape->T_max ? n_stream : shape->T_max);
-  int n_split, kps;
-  decode_plan(shape->B, shape->H_kv, static_cast<int>(a_max), &n_split, &kps);
+  const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
   DecodeArgs a{};
   a.q = q;
   a.k = k;
@@ -103,8 +102,9 @@ int sparse_attn_decode_noalloc(const void *q, const void *k, const void *v,
   a.H_kv = shape->H_kv;
   a.D = shape->D;
   a.dtype = shape->dtype;
-  a.n_split = n_split;
-  a.keys_per_split = kps;
+  a.n_split = plan.n_split;
+  a.keys_per_split = plan.keys_per_split;
+  a.cluster = plan.cluster;
   a.part = part;
   a.out = out;
   a.lse = lse;

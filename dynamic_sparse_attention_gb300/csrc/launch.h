@@ -55,14 +55,29 @@ struct DecodeArgs {
   float scale;
   int B, T_max, T_q, H_q, H_kv, D, dtype;
   int n_split, keys_per_split;
+  bool cluster;           // plan path (see DecodePlan)
   float *part;            // [B, n_split, T_q, H_q, D + 2]
   void *out;
   float *lse;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
 
-// Decode split plan shared by the workspace query and the launch.
-void decode_plan(int B, int H_kv, int a_max, int *n_split, int *keys_per_split);
+// Decode plan shared by the workspace query and the launch.
+//  * cluster path (cluster = true): one thread-block cluster of n_split CTAs per
+//    (batch row, KV head), keys_per_split keys per CTA, tensor-core tiles, merged in
+//    distributed shared memory; needs no workspace.  bf16 with R = (H_q/H_kv)*T_q
+//    <= 16 query rows per KV head.
+//  * split path: n_split CTAs per (b, g) write partials to the workspace, a second
+//    kernel merges them.
+struct DecodePlan {
+  bool cluster;
+  int n_split;
+  int keys_per_split;
+};
+DecodePlan decode_plan(int B, int H_kv, int R, int D, int dtype, int a_max);
+cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t s);
+// workspace floats of the split path (0 on the cluster path)
+size_t decode_ws_floats(const DecodePlan &p, int B, int T_q, int H_q, int D);
 
 // Vertical-slash index build.
 struct VsArgs {
