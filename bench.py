@@ -34,6 +34,12 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn decode μs/step @1M ctx; prefill ms @128K; % HBM / TC roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# DRAM bytes read + written per launch, from ncu captures of the kernels as they are
+# now (profiles/hip_stage_score_s0_decode_1m.md, profiles/prefill_attention_tc_S131072.md);
+# keyed by (kernel, workload).  Remove an entry when its kernel changes.
+NCU_TRAFFIC = {
+    ("hip_stage_score_s0", "decode_gqa_T1048576"): 200653824 + 5608192,
+}
 
 
 def parse_args():
@@ -438,7 +444,8 @@ def main():
     dom_bytes = dec_kernel_bytes.get(dom)
     achieved = dom_bytes / (kern[dom]["avg_us"] * 1e-6) / 1e9 if dom_bytes else None
     roofline = {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s",
-                "frac": achieved / hbm if achieved else None, "traffic": None,
+                "frac": achieved / hbm if achieved else None,
+                "traffic": NCU_TRAFFIC.get((dom, dec.name)),
                 "peak_source": f"{peaks_src} hbm_gbs",
                 "algorithmic_bytes_per_launch": dom_bytes}
 
@@ -457,7 +464,8 @@ def main():
     vs_bytes = accounting.vs_index_bytes(1, pre.S, pre.H_q, pre.H_kv, pre.D, pre.n_vertical)
     vs_us = sum(kern[n]["avg_us"] for n in kern if n.startswith("vs_"))
     roofline_prefill = {"kernel": att_name, "bound": "tensor", "achieved": tflops, "peak": tc_peak,
-                        "unit": "TFLOP/s", "frac": tflops / tc_peak, "traffic": None,
+                        "unit": "TFLOP/s", "frac": tflops / tc_peak,
+                        "traffic": NCU_TRAFFIC.get((att_name, pre.name)),
                         "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)",
                         "algorithmic_flops_per_launch": flops}
 

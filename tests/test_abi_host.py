@@ -81,8 +81,14 @@ def test_workspace_sizes(lib):
     m = ctypes.c_int()
     assert lib.dsa_hip_max_chunks(ctypes.byref(s), ctypes.byref(c), 0, ctypes.byref(m)) == 0
     assert m.value == (1048576 - 128 - 1024 + 255) // 256
+    # bf16 with <= 16 query rows per KV head: the cluster kernel merges in shared memory
     assert lib.sparse_attn_decode_workspace(ctypes.byref(s), 4096, 128, 1024, ctypes.byref(n)) == 0
-    assert n.value > 0
+    assert n.value == 0
+    # fp32, or more than 16 rows per KV head: split-K partials in the workspace
+    for kw in ({"dtype": 1}, {"T_q": 8}):
+        s2 = _shape(T_max=1 << 20, **kw)
+        assert lib.sparse_attn_decode_workspace(ctypes.byref(s2), 4096, 128, 1024, ctypes.byref(n)) == 0
+        assert n.value > 0
 
 
 def test_null_and_misaligned_pointers_rejected(lib):
