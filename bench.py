@@ -39,6 +39,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # keyed by (kernel, workload).  Remove an entry when its kernel changes.
 NCU_TRAFFIC = {
     ("hip_stage_score_s0", "decode_gqa_T1048576"): 200653824 + 5608192,
+    ("prefill_attention_tc", "prefill_vs_S131072"): 4342883328 + 1074967552,
 }
 
 
