@@ -8,6 +8,12 @@ namespace dsa {
 
 constexpr unsigned kFull = 0xffffffffu;
 
+// Programmatic dependent launch: a kernel launched with launch_pdl may be scheduled
+// while the previous kernel of the stream drains; it must call grid_dep_wait() before
+// it reads anything an earlier kernel wrote or writes anything an earlier kernel
+// reads.  A kernel launched the ordinary way returns from it at once.
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 __device__ __forceinline__ float bf16_to_f32(uint16_t h) {

@@ -79,6 +79,7 @@ __global__ void __launch_bounds__(kNT) decode_splitk_kernel(DecodeArgs a) {
   float *s_l = s_m + R;
   float *s_alpha = s_l + R;
 
+  grid_dep_wait();
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Tb = min(max(a.kv_len[b], 0), a.T_max);
@@ -219,6 +220,7 @@ __global__ void __launch_bounds__(kNT) decode_splitk_kernel(DecodeArgs a) {
 
 template <typename T, int D>
 __global__ void decode_merge_kernel(DecodeArgs a) {
+  grid_dep_wait();
   const int row = blockIdx.x;                 // (b, t, h)
   const int per_b = a.T_q * a.H_q;
   const int b = row / per_b, th = row - b * per_b;
@@ -257,13 +259,13 @@ cudaError_t launch_decode_t(const DecodeArgs &a, cudaStream_t s) {
   dim3 grid(a.n_split, a.H_kv, a.B);
   {
     ProfScope ps("decode_splitk", s);
-    kern<<<grid, kNT, smem, s>>>(a);
+    launch_pdl(kern, grid, dim3(kNT), smem, s, a);
   }
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   {
     ProfScope ps("decode_merge", s);
-    decode_merge_kernel<T, D><<<a.B * a.T_q * a.H_q, D, 0, s>>>(a);
+    launch_pdl(decode_merge_kernel<T, D>, dim3(a.B * a.T_q * a.H_q), dim3(D), 0, s, a);
   }
   return cudaGetLastError();
 }

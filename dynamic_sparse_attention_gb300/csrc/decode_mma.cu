@@ -86,6 +86,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   int *s_pos = reinterpret_cast<int *>(ring + kWarps * kNBuf * SM::kSlot);
   float *s_part = reinterpret_cast<float *>(s_pos + a.keys_per_split);   // [kWarps + 1][R][D + 2]
 
+  grid_dep_wait();
   cg::cluster_group cluster = cg::this_cluster();
   const int rank = static_cast<int>(cluster.block_rank());
   const int C = static_cast<int>(cluster.num_blocks());
@@ -374,13 +375,16 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
   cfg.blockDim = dim3(kThreads, 1, 1);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = a.n_split;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // may start while the selection's last kernel drains (grid_dep_wait in the kernel)
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;   // the occupancy query below sees the cluster shape only
   // a device that cannot co-schedule 16 CTAs of this size gets clusters of 8
   if (a.n_split > 8) {
     int n_clusters = 0;
@@ -392,6 +396,7 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
       attr[0].val.clusterDim.x = 8;
     }
   }
+  cfg.numAttrs = 2;
   {
     ProfScope ps("decode_cluster_mma", s);
     e = cudaLaunchKernelEx(&cfg, kern, a);

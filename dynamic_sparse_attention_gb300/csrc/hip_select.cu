@@ -65,6 +65,7 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
   int *s_pos = reinterpret_cast<int *>(smem + score_smem_pos_off());
   float *s_q = reinterpret_cast<float *>(smem + score_smem_q_off(a.in_idx != nullptr, a.L));
 
+  grid_dep_wait();
   const int b = blockIdx.y, j = blockIdx.x;
   const InputRange ir = stage_input(a.kv_len, b, a.T_max, a.n_sink, a.n_stream, a.in_idx,
                                     a.in_cnt, a.in_stride);
@@ -170,6 +171,7 @@ __global__ void __launch_bounds__(kTopkThreads) stage_topk_kernel(StageTopkArgs 
   __shared__ uint32_t s_hist[256];
   __shared__ uint32_t s_res[2];
   __shared__ int s_warp[NT / 32 + 1];
+  grid_dep_wait();
   const int b = blockIdx.x, tid = threadIdx.x;
   const InputRange ir = stage_input(a.kv_len, b, a.T_max, a.n_sink, a.n_stream, a.in_idx,
                                     a.in_cnt, a.in_stride);
@@ -280,6 +282,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
   __shared__ uint32_t s_misc[8];   // 0 min, 1 max, 2 boundary bucket, 3 count above, 4 candidates
   __shared__ uint32_t s_hist8[256];
   __shared__ uint32_t s_res[2];
+  grid_dep_wait();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i0 = tid * NPT;
   // the row's scores come in while the candidate range is read (slots past the row's
@@ -557,7 +560,7 @@ cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
   if (a.max_chunks == 0) return cudaSuccess;
   auto go = [&](auto kern) {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<grid, threads, smem, s>>>(a);
+    launch_pdl(kern, grid, dim3(threads), smem, s, a);
   };
   // fp32 rows need twice the registers: six CTAs per SM there
   if (qreg && threads <= 256) go(stage_score_kernel<T, D, true, 256, sizeof(T) == 2 ? 8 : 6>);
@@ -581,7 +584,7 @@ cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s) {
   auto go = [&](auto kern, int threads, size_t static_bytes) {
     if (smem + static_bytes > 48 * 1024)
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    kern<<<a.B, threads, smem, s>>>(a);
+    launch_pdl(kern, dim3(a.B), dim3(threads), smem, s, a);
   };
   // 16-byte list access needs 16-byte aligned rows of the explicit input list, and rows
   // holding whole chunks (the last chunk's 16-byte groups then stay inside the row)

@@ -8,6 +8,24 @@
 
 namespace dsa {
 
+// Launch with programmatic stream serialization allowed: the grid may start while
+// the stream's previous kernel drains (its CTAs then wait in grid_dep_wait()).
+template <typename Kern, typename... Args>
+cudaError_t launch_pdl(Kern kern, dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, args...);
+}
+
 // One pruning stage's chunk scoring (SelectRep tournament + max over heads).
 struct StageScoreArgs {
   const void *q;          // [B, T_q, H_q, D]
