@@ -37,8 +37,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # DRAM bytes read + written per launch, from ncu captures of the kernels as they are
 # now (profiles/hip_stage_score_s0_decode_1m.md, profiles/prefill_attention_tc_S131072.md);
 # keyed by (kernel, workload).  Remove an entry when its kernel changes.
+# refresh intervals per pruning stage for the mask-caching measurement: the pages' three-stage
+# presets (InfiniteHiP section 3.4, default 16/8/4 and "flash" 96/24/8) with the fourth,
+# finest stage refreshed together with the third
+CACHE_PRESETS = {"default": (16, 8, 4, 4), "flash": (96, 24, 8, 8)}
 NCU_TRAFFIC = {
-    ("hip_stage_score_s0", "decode_gqa_T1048576"): 200653824 + 5608192,
+    ("hip_stage_score_s0", "decode_gqa_T1048576"): 200670720 + 5314560,
     ("prefill_attention_tc", "prefill_vs_S131072"): 4342883328 + 1074967552,
 }
 
@@ -395,6 +399,54 @@ def main():
     torch.cuda.synchronize()
     eager = [a.elapsed_time(b) for a, b in eager]
 
+    # ---------------- mask caching: amortized decode step over one refresh period
+    c_idx, c_cnt = torch.empty_like(sel_idx), torch.empty_like(sel_cnt)
+    ws_cache = torch.empty_like(ws_sel)
+
+    def cached_step(mask):
+        dsa.hip_select_cached(q, k, kv_len, cfg, mask, out=(c_idx, c_cnt), workspace=ws_cache)
+        dsa.sparse_attn_decode(q, k, v, kv_len, c_idx, c_cnt, n_sink=dec.n_sink,
+                               n_stream=dec.n_stream, out=out, lse=lse, workspace=ws_dec)
+
+    cached = {}
+    cache_graphs = {}
+    for name, n_refresh in CACHE_PRESETS.items():
+        if len(n_refresh) != len(dec.chunk):
+            continue
+        period = n_refresh[0]
+        masks = [dsa.refresh_mask(s, n_refresh) for s in range(period)]
+        for m in sorted(set(masks)):
+            if m in cache_graphs:
+                continue
+            side.wait_stream(torch.cuda.current_stream())
+            with torch.cuda.stream(side):
+                cached_step(m)
+            torch.cuda.current_stream().wait_stream(side)
+            torch.cuda.synchronize()
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cached_step(m)
+            cache_graphs[m] = g
+        by_mask = {}
+        reps = max(1, 32 // period)
+        for _ in range(reps):
+            for m in masks:
+                flush()
+                e0, e1 = ev(), ev()
+                e0.record()
+                cache_graphs[m].replay()
+                e1.record()
+                by_mask.setdefault(m, []).append((e0, e1))
+        torch.cuda.synchronize()
+        us = {m: [1e3 * a.elapsed_time(b) for a, b in v_] for m, v_ in by_mask.items()}
+        total = sum(sum(v_) for v_ in us.values())
+        cached[name] = {
+            "n_refresh": list(n_refresh), "period_steps": period, "periods_timed": reps,
+            "us_per_step_amortized": total / (reps * period),
+            "us_by_refreshed_stages": {",".join(str(i) for i in range(len(n_refresh)) if m >> i & 1)
+                                       or "none": statistics.mean(v_) for m, v_ in us.items()},
+        }
+
     # ---------------- per-kernel durations (CUDA events on the launch stream)
     dsa.profile_enable(True)
     for _ in range(args.steps):
@@ -561,6 +613,9 @@ def main():
             "chunks_per_stage": stage_chunks,
             "attended_keys": attended,
         },
+        # mask caching (InfiniteHiP section 3.4): the same step with stage i recomputed only
+        # when step % n_refresh[i] == 0, averaged over whole refresh periods
+        "decode_cached": cached,
         "prefill": {
             "ms": pre_ms,
             "vs_index_ms": statistics.mean(idx_ms),

@@ -12,11 +12,14 @@ from .binding import (  # noqa: F401
     HipConfig,
     hip_max_chunks,
     hip_select,
+    hip_select_cached,
+    HipSelectCache,
     hip_select_workspace_bytes,
     library_path,
     load,
     profile_collect,
     profile_enable,
+    refresh_mask,
     sparse_attn_decode,
     sparse_attn_decode_noalloc,
     sparse_attn_decode_workspace_bytes,

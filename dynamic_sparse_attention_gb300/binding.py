@@ -71,6 +71,8 @@ _SIGNATURES = {
     "dsa_hip_max_chunks": (_c_int, [_vp, _vp, _c_int, ctypes.POINTER(_c_int)]),
     "hip_select_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
     "hip_select": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "hip_select_cached": (_c_int, [_vp, _vp, _vp, _vp, _vp, ctypes.c_uint32, _vp, _vp, _vp, _vp,
+                                   ctypes.c_size_t, _vp]),
     "sparse_attn_decode_workspace": (_c_int, [_vp, _c_int, _c_int, _c_int,
                                               ctypes.POINTER(ctypes.c_size_t)]),
     "sparse_attn_decode": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
@@ -226,6 +228,61 @@ def hip_max_chunks(q, k, cfg: HipConfig, stage: int) -> int:
 def hip_select(q, k, kv_len, cfg: HipConfig, *, debug: bool = False, out=None, workspace=None,
                stream=None):
     """Run all pruning stages; returns (sel_idx [B, keep[-1]], sel_cnt [B][, debug dict])."""
+    return _hip_select(q, k, kv_len, cfg, None, debug, out, workspace, stream)
+
+
+def hip_select_cached(q, k, kv_len, cfg: HipConfig, refresh: int, *, out, workspace,
+                      debug: bool = False, stream=None):
+    """Recompute only the pruning stages whose bit is set in `refresh` (InfiniteHiP,
+    section 3.4 "Sparse Attention Mask Caching"); the others keep the lists they left in
+    `workspace` / `out` on an earlier call, so both must persist between calls.
+    Returns like hip_select (debug tensors of skipped stages stay at their fill)."""
+    if out is None or workspace is None:
+        raise ValueError("hip_select_cached needs the persistent out buffers and workspace")
+    return _hip_select(q, k, kv_len, cfg, int(refresh), debug, out, workspace, stream)
+
+
+def refresh_mask(step: int, n_refresh) -> int:
+    """Stages to recompute at decoding step `step` (counted from 0) when stage i is
+    refreshed every n_refresh[i] steps (InfiniteHiP, section 3.4): bit i is set iff
+    step % n_refresh[i] == 0, so step 0 recomputes every stage."""
+    m = 0
+    for i, r in enumerate(n_refresh):
+        if int(r) <= 0:
+            raise ValueError("refresh intervals must be positive")
+        if step % int(r) == 0:
+            m |= 1 << i
+    return m
+
+
+class HipSelectCache:
+    """Decoding-loop helper for mask caching: owns the workspace and the selection
+    buffers, keeps the step counter and recomputes, on each call, the stages whose
+    refresh interval divides it.  Shapes and config are fixed at construction."""
+
+    def __init__(self, q, k, cfg: HipConfig, n_refresh):
+        if len(n_refresh) != len(cfg.chunk):
+            raise ValueError("one refresh interval per pruning stage")
+        refresh_mask(0, n_refresh)
+        self.cfg = cfg
+        self.n_refresh = tuple(int(r) for r in n_refresh)
+        B = q.shape[0]
+        self.sel_idx = torch.empty(B, cfg.keep[-1], dtype=torch.int32, device=q.device)
+        self.sel_cnt = torch.empty(B, dtype=torch.int32, device=q.device)
+        self.workspace = _workspace(hip_select_workspace_bytes(q, k, cfg), q.device, None)
+        self.step = 0
+
+    def mask(self, step=None) -> int:
+        return refresh_mask(self.step if step is None else step, self.n_refresh)
+
+    def __call__(self, q, k, kv_len, *, debug: bool = False, stream=None):
+        m = self.mask()
+        self.step += 1
+        return hip_select_cached(q, k, kv_len, self.cfg, m, out=(self.sel_idx, self.sel_cnt),
+                                 workspace=self.workspace, debug=debug, stream=stream)
+
+
+def _hip_select(q, k, kv_len, cfg, refresh, debug, out, workspace, stream):
     lib = load()
     _need_cuda(q, k, kv_len)
     shape, c = decode_shape(q, k), cfg.c()
@@ -255,10 +312,16 @@ def hip_select(q, k, kv_len, cfg: HipConfig, *, debug: bool = False, out=None, w
                 getattr(dbg, key)[i] = v.data_ptr()
     nbytes = hip_select_workspace_bytes(q, k, cfg)
     ws = _workspace(nbytes, dev, workspace)
-    st = lib.hip_select(_ptr(q), _ptr(k), _ptr(kv_len), ctypes.byref(shape), ctypes.byref(c),
-                        _ptr(sel_idx), _ptr(sel_cnt), ctypes.byref(dbg) if dbg else None,
-                        _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
-    _check("hip_select", st)
+    dbg_p = ctypes.byref(dbg) if dbg else None
+    if refresh is None:
+        st = lib.hip_select(_ptr(q), _ptr(k), _ptr(kv_len), ctypes.byref(shape), ctypes.byref(c),
+                            _ptr(sel_idx), _ptr(sel_cnt), dbg_p, _ptr(ws),
+                            ctypes.c_size_t(ws.numel()), _stream(stream))
+    else:
+        st = lib.hip_select_cached(_ptr(q), _ptr(k), _ptr(kv_len), ctypes.byref(shape),
+                                   ctypes.byref(c), refresh, _ptr(sel_idx), _ptr(sel_cnt),
+                                   dbg_p, _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check("hip_select" if refresh is None else "hip_select_cached", st)
     if debug:
         return sel_idx, sel_cnt, dbg_t
     return sel_idx, sel_cnt

@@ -124,13 +124,17 @@ int hip_select_workspace(const dsa_decode_shape *shape, const dsa_hip_cfg *cfg, 
   return DSA_OK;
 }
 
-int hip_select(const void *q, const void *k, const int32_t *kv_len, const dsa_decode_shape *shape,
-               const dsa_hip_cfg *cfg, int32_t *sel_idx, int32_t *sel_cnt,
-               const dsa_hip_debug *dbg, void *ws, size_t ws_bytes, void *stream) {
+int hip_select_cached(const void *q, const void *k, const int32_t *kv_len,
+                      const dsa_decode_shape *shape, const dsa_hip_cfg *cfg, uint32_t refresh,
+                      int32_t *sel_idx, int32_t *sel_cnt, const dsa_hip_debug *dbg, void *ws,
+                      size_t ws_bytes, void *stream) {
   clear_error();
   int st = check_decode_shape(shape);
   if (st) return st;
   if ((st = check_hip_cfg(shape, cfg))) return st;
+  if (refresh >> cfg->n_stages)
+    return fail(DSA_ERR_INVALID_ARG, "refresh mask 0x%x has bits at or above n_stages=%d", refresh,
+                cfg->n_stages);
   if (!aligned(q, 16) || !aligned(k, 16))
     return fail(DSA_ERR_ALIGNMENT, "q and k must be non-NULL and 16-byte aligned");
   if (!aligned(kv_len, 4) || !aligned(sel_idx, 4) || !aligned(sel_cnt, 4))
@@ -143,6 +147,7 @@ int hip_select(const void *q, const void *k, const int32_t *kv_len, const dsa_de
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int n = cfg->n_stages;
   for (int i = 0; i < n; ++i) {
+    if (!((refresh >> i) & 1u)) continue;   // cached: the stage's list in ws (or sel_idx) stays
     const int maxc = max_chunks(shape, cfg, i);
     StageScoreArgs sa{};
     sa.q = q;
@@ -198,6 +203,15 @@ int hip_select(const void *q, const void *k, const int32_t *kv_len, const dsa_de
     if (e != cudaSuccess) return cuda_fail(e, "stage_topk launch");
   }
   return DSA_OK;
+}
+
+int hip_select(const void *q, const void *k, const int32_t *kv_len, const dsa_decode_shape *shape,
+               const dsa_hip_cfg *cfg, int32_t *sel_idx, int32_t *sel_cnt,
+               const dsa_hip_debug *dbg, void *ws, size_t ws_bytes, void *stream) {
+  const bool ok = cfg && cfg->n_stages >= 1 && cfg->n_stages <= DSA_MAX_STAGES;
+  const uint32_t all = ok ? (1u << cfg->n_stages) - 1u : 0u;   // a bad cfg fails in the callee
+  return hip_select_cached(q, k, kv_len, shape, cfg, all, sel_idx, sel_cnt, dbg, ws, ws_bytes,
+                           stream);
 }
 
 int sparse_attn_decode_workspace(const dsa_decode_shape *shape, int max_sel, int n_sink,

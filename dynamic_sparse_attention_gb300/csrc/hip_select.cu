@@ -74,8 +74,8 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
   const int base = j * a.L;
   const int len = min(a.L, ir.n_in - base);
   const T *q = static_cast<const T *>(a.q) + static_cast<size_t>(b) * a.T_q * a.H_q * D;
-  if (ir.in) {
-    for (int x = threadIdx.x; x < len; x += blockDim.x) s_pos[x] = ir.in[base + x];
+  if (ir.in) {   // a cached list may be stale: never read outside the key rows
+    for (int x = threadIdx.x; x < len; x += blockDim.x) s_pos[x] = min(max(ir.in[base + x], 0), a.T_max - 1);
   }
   if (!QREG) {
     const int n = a.T_q * a.H_q * D;

@@ -121,6 +121,27 @@ int hip_select(const void *q, const void *k, const int32_t *kv_len,
                int32_t *sel_idx, int32_t *sel_cnt, const dsa_hip_debug *dbg,
                void *ws, size_t ws_bytes, void *stream);
 
+/* hip_select_cached -- hip_select with per-stage mask caching (InfiniteHiP, section 3.4
+ * "Sparse Attention Mask Caching"): pruning stage i is recomputed only when bit i of
+ * `refresh` is set -- a decoding loop sets it when step % n_refresh[i] == 0 -- and a
+ * stage that is not refreshed keeps the token list it produced on an earlier call.
+ * A refreshed stage i > 0 starts from the list stage i-1 holds at that moment (just
+ * recomputed, or cached); stage 0 always starts from the full candidate range of the
+ * current kv_len.  Lists of stages 0..n_stages-2 live in `ws`, the last stage's in
+ * sel_idx / sel_cnt, so all three must be the same buffers, unchanged by the caller,
+ * from one call to the next; refresh = (1 << n_stages) - 1 is exactly hip_select and
+ * refresh = 0 launches nothing.  Cached lists are not re-validated: positions read back
+ * are clamped to [0, T_max) before any key row is read, and counts to [0, keep[i]], so
+ * a workspace that holds no earlier selection gives a meaningless selection but never
+ * an access outside k or ws.  A context that grew since stage 0 last ran keeps that
+ * stage's candidates: tokens that left the streaming window in between are attended
+ * again only after the next refresh of stage 0.
+ * Errors as for hip_select; a bit at or above n_stages is INVALID_ARG. */
+int hip_select_cached(const void *q, const void *k, const int32_t *kv_len,
+                      const dsa_decode_shape *shape, const dsa_hip_cfg *cfg, uint32_t refresh,
+                      int32_t *sel_idx, int32_t *sel_cnt, const dsa_hip_debug *dbg, void *ws,
+                      size_t ws_bytes, void *stream);
+
 /* Bytes of scratch sparse_attn_decode needs (split-K partials) (host only). */
 int sparse_attn_decode_workspace(const dsa_decode_shape *shape, int max_sel, int n_sink,
                                  int n_stream, size_t *bytes);

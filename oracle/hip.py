@@ -199,6 +199,44 @@ def hip_select(q, K, dtype, T, chunk, keep, n_sink, n_stream, G):
     return stages, I
 
 
+# ---------------------------------------------------------------- mask caching
+
+def refresh_schedule(step: int, n_refresh) -> list:
+    """Which stages recompute their output at decoding step `step` (counted from 0).
+
+    Section 3.4 "Sparse Attention Mask Caching (Temporal Locality Exploitation)":
+    stage i has a refresh interval n_refresh[i]; its stored output is recomputed when
+    the step counter is a multiple of that interval and reused unchanged otherwise.
+    """
+    return [step % int(r) == 0 for r in n_refresh]
+
+
+def hip_select_cached(q, K, dtype, T, chunk, keep, n_sink, n_stream, G, refresh, cache):
+    """One decoding step of the pruning pipeline with per-stage mask caching, one row.
+
+    Same section as refresh_schedule.  `cache[i]` holds stage i's stored output list
+    (None before it first ran) and is updated in place for the stages with
+    refresh[i] true; the others are skipped.  A recomputed stage 0 prunes the
+    candidate range of the current context length T; a recomputed stage i > 0 prunes
+    cache[i-1] as it stands at that point of the step (recomputed just before, or
+    cached).  Returns ({stage: StageResult} for the recomputed stages, cache[-1]).
+    """
+    ran = {}
+    for i, (L, k) in enumerate(zip(chunk, keep)):
+        if not refresh[i]:
+            continue
+        if i == 0:
+            I = candidate_range(T, n_sink, n_stream)
+        else:
+            if cache[i - 1] is None:
+                raise ValueError(f"stage {i} refreshed before stage {i - 1} ever ran")
+            I = cache[i - 1]
+        st = pruning_stage(q, K, dtype, I, L, k, G)
+        cache[i] = st.I_out
+        ran[i] = st
+    return ran, cache[-1]
+
+
 # ---------------------------------------------------------------- attention
 
 def decode_attention(q, K, V, dtype, A, scale, G):

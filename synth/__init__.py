@@ -9,6 +9,7 @@ from .workloads import (  # noqa: F401
     PrefillCase,
     f32_to_bf16_bits,
     decode_case,
+    decode_steps,
     prefill_case,
     decode_tiny,
     decode_128k,

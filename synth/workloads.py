@@ -203,6 +203,25 @@ def decode_batch16() -> DecodeCase:
                        seeds_per_row=[300 + b for b in range(16)])
 
 
+def decode_steps(case: DecodeCase, n_steps: int, seed: int, drift: float = 0.3):
+    """A seeded decoding loop over one case: per step s a query block
+    q_s = case.q + drift * N(0,1) (rounded to the case's storage type) and kv_len_s =
+    min(case.kv_len + s, T_max), i.e. one new token per step in every row.  Returns a
+    list of (q_s, kv_len_s); step 0 uses case.q itself."""
+    bf16 = case.dtype == "bf16"
+    rng = np.random.default_rng(seed)
+    base = _as_f32(case.q, bf16)
+    out = []
+    for s in range(n_steps):
+        if s == 0:
+            q = case.q.copy()
+        else:
+            q = _store(base + drift * rng.standard_normal(base.shape, dtype=np.float32), bf16)
+        kv = np.minimum(case.kv_len.astype(np.int64) + s, case.T_max).astype(np.int32)
+        out.append((q, kv))
+    return out
+
+
 # --------------------------------------------------------------------------- prefill
 
 def prefill_case(name, *, B=1, S, H_q, H_kv, D, seed, last_q=64, n_vertical=1000,

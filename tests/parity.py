@@ -121,38 +121,42 @@ def check_topk(s_gpu32, s64, K, kept_gpu, D):
     return int(np.sum(kept != np.isin(np.arange(n), order[:K])))
 
 
+def check_hip_stage(case, b, dbg, i, I, stats):
+    """Replay pruning stage i of batch row b from the input list I against the GPU's
+    debug outputs of that stage; returns the GPU's (validated) output list."""
+    q64 = to_f64(case.q[b], case.dtype)
+    L, keep = case.chunk[i], case.keep[i]
+    chunks = hip.chunk_partition(np.asarray(I, np.int64), L)
+    n = len(chunks)
+    cnt = int(dbg["stage_cnt"][i][b])
+    lst = dbg["stage_idx"][i][b].cpu().numpy()
+    if n == 0:
+        assert cnt == 0 and np.all(lst == -1)
+        return np.zeros(0, np.int64)
+    reps = dbg["rep"][i][b, :, :n].cpu().numpy().astype(np.int64)
+    rho = dbg["rep_score"][i][b, :, :n].cpu().numpy()
+    s_gpu = dbg["chunk_score"][i][b, :n].cpu().numpy()
+    rho64, flips = check_tournament(q64, case.k[b], case.dtype, chunks, reps, rho, case.G, case.D)
+    stats["flips"] += flips
+    assert np.array_equal(s_gpu, rho.max(axis=0)), "chunk score is not the max over heads"
+    s64 = rho64.max(axis=0)
+    # kept chunks from the GPU list
+    got = lst[:cnt].astype(np.int64)
+    assert np.all(lst[cnt:] == -1), "list not padded with -1"
+    pos_in = {int(p): x for x, p in enumerate(I)}
+    kept_gpu = np.unique([pos_in[int(p)] // L for p in got]) if cnt else np.zeros(0, np.int64)
+    stats["band_diffs"] += check_topk(s_gpu, s64, keep // L, kept_gpu, case.D)
+    want_list = hip.assemble(chunks, kept_gpu)
+    assert np.array_equal(got, want_list), "assembled list differs"
+    return got
+
+
 def check_hip_row(case, b, dbg, sel_idx, sel_cnt):
     """Full replay check of one batch row's pruning stages; returns the GPU's final list."""
-    q64 = to_f64(case.q[b], case.dtype)
-    K = case.k[b]
-    T = int(case.kv_len[b])
-    I = hip.candidate_range(T, case.n_sink, case.n_stream)
+    I = hip.candidate_range(int(case.kv_len[b]), case.n_sink, case.n_stream)
     stats = {"flips": 0, "band_diffs": 0}
-    for i, (L, keep) in enumerate(zip(case.chunk, case.keep)):
-        chunks = hip.chunk_partition(I, L)
-        n = len(chunks)
-        cnt = int(dbg["stage_cnt"][i][b])
-        lst = dbg["stage_idx"][i][b].cpu().numpy()
-        if n == 0:
-            assert cnt == 0 and np.all(lst == -1)
-            I = np.zeros(0, np.int64)
-            continue
-        reps = dbg["rep"][i][b, :, :n].cpu().numpy().astype(np.int64)
-        rho = dbg["rep_score"][i][b, :, :n].cpu().numpy()
-        s_gpu = dbg["chunk_score"][i][b, :n].cpu().numpy()
-        rho64, flips = check_tournament(q64, K, case.dtype, chunks, reps, rho, case.G, case.D)
-        stats["flips"] += flips
-        assert np.array_equal(s_gpu, rho.max(axis=0)), "chunk score is not the max over heads"
-        s64 = rho64.max(axis=0)
-        # kept chunks from the GPU list
-        got = lst[:cnt].astype(np.int64)
-        assert np.all(lst[cnt:] == -1), "list not padded with -1"
-        pos_in = {int(p): x for x, p in enumerate(I)}
-        kept_gpu = np.unique([pos_in[int(p)] // L for p in got]) if cnt else np.zeros(0, np.int64)
-        stats["band_diffs"] += check_topk(s_gpu, s64, keep // L, kept_gpu, case.D)
-        want_list = hip.assemble(chunks, kept_gpu)
-        assert np.array_equal(got, want_list), "assembled list differs"
-        I = got
+    for i in range(len(case.chunk)):
+        I = check_hip_stage(case, b, dbg, i, I, stats)
     final = sel_idx[b, :int(sel_cnt[b])].cpu().numpy().astype(np.int64)
     assert np.array_equal(final, I)
     return I, stats

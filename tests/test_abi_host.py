@@ -114,3 +114,30 @@ def test_null_and_misaligned_pointers_rejected(lib):
     st = lib.sparse_attn_decode(ok, ok, ok, ok, ok, ok, 16, 4, 4, ctypes.c_float(float("nan")),
                                 ctypes.byref(s), ok, None, ok, ctypes.c_size_t(1 << 30), None)
     assert st == -1
+
+
+def test_hip_select_cached_validates_the_refresh_mask(lib):
+    s = _shape()
+    c = _cfg()   # four stages
+    buf = (ctypes.c_char * 64)()
+    ok = ctypes.c_void_p(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 16))
+    for mask in (1 << 4, 0xFFFFFFFF, 1 << 31):
+        st = lib.hip_select_cached(ok, ok, ok, ctypes.byref(s), ctypes.byref(c),
+                                   ctypes.c_uint32(mask), ok, ok, None, ok,
+                                   ctypes.c_size_t(1 << 30), None)
+        assert st == -1
+        assert b"refresh mask" in lib.dsa_last_error()
+    # a valid mask gets as far as the workspace check (no launch)
+    st = lib.hip_select_cached(ok, ok, ok, ctypes.byref(s), ctypes.byref(c), ctypes.c_uint32(0b0110),
+                               ok, ok, None, ok, ctypes.c_size_t(8), None)
+    assert st == -3
+
+
+def test_refresh_mask_helper():
+    assert binding.refresh_mask(0, (16, 8, 4, 4)) == 0b1111
+    assert binding.refresh_mask(4, (16, 8, 4, 4)) == 0b1100
+    assert binding.refresh_mask(8, (16, 8, 4, 4)) == 0b1110
+    assert binding.refresh_mask(5, (16, 8, 4, 4)) == 0
+    assert binding.refresh_mask(48, (96, 24, 8, 8)) == 0b1110
+    with pytest.raises(ValueError):
+        binding.refresh_mask(3, (4, 0))

@@ -1,4 +1,6 @@
 """GPU parity of the decode half (hip_select + sparse_attn_decode) against the fp64 oracle."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -7,8 +9,8 @@ import dynamic_sparse_attention_gb300 as dsa
 from dynamic_sparse_attention_gb300 import _build
 from oracle import hip
 from oracle.numerics import to_f64
-from parity import attention_errors, check_hip_row, from_dev_bits, to_dev
-from synth import decode_128k, decode_batch16, decode_case, decode_tiny
+from parity import attention_errors, check_hip_row, check_hip_stage, from_dev_bits, to_dev
+from synth import decode_128k, decode_batch16, decode_case, decode_steps, decode_tiny
 
 pytestmark = pytest.mark.gpu
 
@@ -159,3 +161,115 @@ def test_gqa_128k_config():
 def test_batch16_config():
     """Batch 16 at 32K with one planted cluster per row (checks rows 0, 7 and 15 in full)."""
     _check_case(decode_batch16(), rows=[0, 7, 15])
+
+
+# ------------------------------------------------------------ mask caching (section 3.4)
+
+def _cache_case():
+    return decode_case("decode_cache_B2_T16384", B=2, T=16384, T_q=1, H_q=32, H_kv=8, D=128,
+                       dtype="bf16", chunk=(256, 64, 16, 4), keep=(2048, 1024, 512, 256),
+                       n_sink=64, n_stream=256, seed=50, plant="uniform", n_plant=32,
+                       kv_len=[16000, 11001])
+
+
+def _upload(c):
+    return (to_dev(c.q, c.dtype), to_dev(c.k, c.dtype), to_dev(c.v, c.dtype),
+            torch.from_numpy(c.kv_len).cuda(), dsa.HipConfig(c.chunk, c.keep, c.n_sink, c.n_stream))
+
+
+def test_cached_with_every_stage_is_hip_select():
+    c = _cache_case()
+    q, k, v, kv_len, cfg = _upload(c)
+    ref_idx, ref_cnt, ref_dbg = dsa.hip_select(q, k, kv_len, cfg, debug=True)
+    ws = torch.zeros(dsa.hip_select_workspace_bytes(q, k, cfg), dtype=torch.uint8, device="cuda")
+    out = (torch.full_like(ref_idx, -9), torch.full_like(ref_cnt, -9))
+    idx, cnt, dbg = dsa.hip_select_cached(q, k, kv_len, cfg, 0b1111, out=out, workspace=ws,
+                                          debug=True)
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref_idx) and torch.equal(cnt, ref_cnt)
+    for key in ref_dbg:
+        for a, b in zip(dbg[key], ref_dbg[key]):
+            torch.testing.assert_close(a, b, rtol=0, atol=0, equal_nan=True)
+
+
+def test_cached_without_refresh_changes_nothing():
+    c = _cache_case()
+    q, k, v, kv_len, cfg = _upload(c)
+    cache = dsa.HipSelectCache(q, k, cfg, (4, 2, 1, 1))
+    idx, cnt = cache(q, k, kv_len)
+    before = (idx.clone(), cnt.clone(), cache.workspace.clone())
+    q2 = torch.randn_like(q)
+    dsa.hip_select_cached(q2, k, kv_len + 7, cfg, 0, out=(cache.sel_idx, cache.sel_cnt),
+                          workspace=cache.workspace)
+    torch.cuda.synchronize()
+    assert torch.equal(cache.sel_idx, before[0]) and torch.equal(cache.sel_cnt, before[1])
+    assert torch.equal(cache.workspace, before[2])
+
+
+@pytest.mark.parametrize("n_refresh", [(4, 2, 1, 1), (4, 3, 2, 1)])
+def test_cached_decoding_loop_against_oracle(n_refresh):
+    """Ten decoding steps, one new token and a drifting query per step.  Each refreshed
+    stage is replayed against the oracle from the list the GPU holds for the stage
+    before it (fresh or cached); skipped stages must leave their lists alone; the
+    attention of every step is checked over sink + cached selection + current window.
+    (4, 3, 2, 1) does not nest, so a stage can be refreshed while the one before it
+    stays cached."""
+    c = _cache_case()
+    _, k, v, _, cfg = _upload(c)
+    steps = decode_steps(c, 10, seed=51)
+    cache = None
+    held = [[None] * c.B for _ in c.chunk]
+    for s, (q_np, kv_np) in enumerate(steps):
+        cs = dataclasses.replace(c, q=q_np, kv_len=kv_np)
+        q = to_dev(q_np, c.dtype)
+        kv_len = torch.from_numpy(kv_np).cuda()
+        if cache is None:
+            cache = dsa.HipSelectCache(q, k, cfg, n_refresh)
+        mask = cache.mask()
+        assert mask == hip_refresh_bits(s, n_refresh)
+        idx, cnt, dbg = cache(q, k, kv_len, debug=True)
+        out, _ = dsa.sparse_attn_decode(q, k, v, kv_len, idx, cnt, n_sink=c.n_sink,
+                                        n_stream=c.n_stream)
+        torch.cuda.synchronize()
+        o_gpu = to_f64(from_dev_bits(out), "bf16")
+        stats = {"flips": 0, "band_diffs": 0}
+        for b in range(c.B):
+            T = int(kv_np[b])
+            for i in range(len(c.chunk)):
+                if mask >> i & 1:
+                    I = hip.candidate_range(T, c.n_sink, c.n_stream) if i == 0 else held[i - 1][b]
+                    held[i][b] = check_hip_stage(cs, b, dbg, i, I, stats)
+                else:
+                    assert int(dbg["stage_cnt"][i][b]) == -7, "a cached stage ran"
+            final = idx[b, :int(cnt[b])].cpu().numpy().astype(np.int64)
+            assert np.array_equal(final, held[-1][b])
+            A = hip.attended_set(T, c.n_sink, c.n_stream, final)
+            assert len(np.unique(A)) == len(A)
+            O64, _ = hip.decode_attention(to_f64(q_np[b], c.dtype), c.k[b], c.v[b], c.dtype, A,
+                                          c.scale, c.G)
+            mx, mn = attention_errors(o_gpu[b], O64)
+            assert mx <= MAX_ABS and mn <= MEAN_ABS, f"step {s} row {b}: max {mx:.3e} mean {mn:.3e}"
+
+
+def hip_refresh_bits(step, n_refresh):
+    return sum(1 << i for i, r in enumerate(hip.refresh_schedule(step, n_refresh)) if r)
+
+
+def test_cached_lists_are_clamped_to_the_key_rows():
+    """A workspace that never held a selection (arbitrary ints as cached lists and
+    counts): the later stages and the attention read only rows inside the context."""
+    c = _cache_case()
+    q, k, v, kv_len, cfg = _upload(c)
+    nbytes = dsa.hip_select_workspace_bytes(q, k, cfg)
+    g = torch.Generator(device="cpu").manual_seed(52)
+    junk = torch.randint(-(1 << 31), (1 << 31) - 1, (nbytes // 4,), generator=g, dtype=torch.int64)
+    ws = junk.to(torch.int32).view(torch.uint8).cuda()
+    out = (torch.empty(c.B, c.keep[-1], dtype=torch.int32, device="cuda"),
+           torch.empty(c.B, dtype=torch.int32, device="cuda"))
+    idx, cnt = dsa.hip_select_cached(q, k, kv_len, cfg, 0b1110, out=out, workspace=ws)
+    o, lse = dsa.sparse_attn_decode(q, k, v, kv_len, idx, cnt, n_sink=c.n_sink,
+                                    n_stream=c.n_stream)
+    torch.cuda.synchronize()
+    assert dsa.device_error() == 0
+    assert ((cnt >= 0) & (cnt <= c.keep[-1])).all()
+    assert torch.isfinite(o.float()).all()

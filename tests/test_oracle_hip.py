@@ -250,3 +250,102 @@ def test_partial_chunk_and_short_context():
     # ragged last chunk keeps its true length
     chunks = hip.chunk_partition(np.arange(10, 31), 8)
     assert [len(x) for x in chunks] == [8, 8, 5]
+
+
+# ------------------------------------------------------------ mask caching (section 3.4)
+
+def test_refresh_timeline_matches_figure7_description(golden):
+    g = golden["mask_refresh_timeline"]
+    for i, want in enumerate(g["refresh_steps"]):
+        got = [c for c in range(g["steps"]) if hip.refresh_schedule(c, g["n_refresh"])[i]]
+        assert got == want, f"stage {i + 1}"
+    # every preset of the table nests: a refresh of stage i is also one of each later stage
+    for r in g["presets"].values():
+        for c in range(2 * r[0] + 1):
+            m = hip.refresh_schedule(c, r)
+            assert m == sorted(m), (r, c, m)
+
+
+def _growing_steps(n_steps, T0, T_max, H_q=4, H_kv=2, D=32, seed=40):
+    c = decode_case("cache", B=1, T=T_max, T_q=1, H_q=H_q, H_kv=H_kv, D=D, dtype="f32",
+                    chunk=(32, 8, 2), keep=(256, 64, 16), n_sink=8, n_stream=16, seed=seed)
+    rng = np.random.default_rng(seed + 1)
+    qs = [rng.standard_normal((1, H_q, D)) for _ in range(n_steps)]
+    return c, qs, [T0 + s for s in range(n_steps)]
+
+
+def test_cached_with_every_stage_refreshed_is_the_full_pipeline():
+    c, qs, Ts = _growing_steps(6, 900, 1000)
+    cache = [None] * 3
+    for q, T in zip(qs, Ts):
+        ran, I = hip.hip_select_cached(q, c.k[0], "f32", T, c.chunk, c.keep, c.n_sink,
+                                       c.n_stream, c.G, [True] * 3, cache)
+        stages, I_full = hip.hip_select(q, c.k[0], "f32", T, c.chunk, c.keep, c.n_sink,
+                                        c.n_stream, c.G)
+        assert np.array_equal(I, I_full)
+        for i, st in enumerate(stages):
+            assert np.array_equal(cache[i], st.I_out)
+            assert np.array_equal(ran[i].kept, st.kept)
+
+
+def test_cached_no_refresh_keeps_every_list():
+    c, qs, Ts = _growing_steps(2, 900, 1000)
+    cache = [None] * 3
+    hip.hip_select_cached(qs[0], c.k[0], "f32", Ts[0], c.chunk, c.keep, c.n_sink, c.n_stream,
+                          c.G, [True] * 3, cache)
+    before = [x.copy() for x in cache]
+    ran, I = hip.hip_select_cached(qs[1], c.k[0], "f32", Ts[1], c.chunk, c.keep, c.n_sink,
+                                   c.n_stream, c.G, [False] * 3, cache)
+    assert ran == {} and all(np.array_equal(a, b) for a, b in zip(before, cache))
+    assert I is cache[-1]
+
+
+def test_refreshed_stage_reads_the_cached_previous_stage():
+    """Three key groups, worked out by hand: with query e1 the first two stages keep the
+    chunks of groups A (score 3) and B (score 2) and the last keeps A; a later query e2
+    prefers C (score 3, outside the cached lists) over B (2) over A (0).  Refreshing
+    only the last stage must give B: C would mean it restarted from the full range, A
+    that it reused its own list or the old query."""
+    T, D = 1024, 16
+    K = np.zeros((T, 1, D), np.float32)
+    K[:, 0, 2:] = 0.01 * np.random.default_rng(5).standard_normal((T, D - 2))
+    A, B, C = np.arange(96, 104), np.arange(512, 520), np.arange(800, 808)
+    K[A, 0, 0] = 3.0
+    K[B, 0, 0] = 2.0
+    K[B, 0, 1] = 2.0
+    K[C, 0, 1] = 3.0
+    e1 = np.zeros((1, 1, D))
+    e1[0, 0, 0] = 1.0
+    e2 = np.zeros((1, 1, D))
+    e2[0, 0, 1] = 1.0
+    chunk, keep = (32, 8, 2), (64, 16, 8)
+    cache = [None] * 3
+    _, I0 = hip.hip_select_cached(e1, K, "f32", T, chunk, keep, 0, 0, 1, [True] * 3, cache)
+    assert np.array_equal(cache[1], np.concatenate([A, B]))
+    assert np.array_equal(I0, A)
+    _, I1 = hip.hip_select_cached(e2, K, "f32", T, chunk, keep, 0, 0, 1,
+                                  [False, False, True], cache)
+    assert np.array_equal(I1, B)
+    # refreshing every stage with e2 instead reaches C
+    _, I2 = hip.hip_select_cached(e2, K, "f32", T, chunk, keep, 0, 0, 1, [True] * 3, cache)
+    assert np.array_equal(I2, C)
+
+
+def test_stale_stage0_list_and_the_attended_set():
+    """Stage 0 cached at T0 while the context grows to T: the selection stays inside the
+    candidate range of T0, the attended set has no repeats, and the tokens that left the
+    streaming window in between are not attended until stage 0 runs again."""
+    c, qs, Ts = _growing_steps(9, 900, 1000)
+    cache = [None] * 3
+    n_refresh = (8, 4, 2)
+    for step, (q, T) in enumerate(zip(qs, Ts)):
+        ran, I = hip.hip_select_cached(q, c.k[0], "f32", T, c.chunk, c.keep, c.n_sink,
+                                       c.n_stream, c.G, hip.refresh_schedule(step, n_refresh),
+                                       cache)
+        T0 = Ts[step - step % 8]
+        assert np.all(np.isin(I, hip.candidate_range(T0, c.n_sink, c.n_stream)))
+        A = hip.attended_set(T, c.n_sink, c.n_stream, I)
+        assert len(np.unique(A)) == len(A) == c.n_sink + len(I) + c.n_stream
+        left = np.arange(T0 - c.n_stream, T - c.n_stream)
+        assert not np.isin(left, A).any()
+        assert (0 in ran) == (step % 8 == 0)
