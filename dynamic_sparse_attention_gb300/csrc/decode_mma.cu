@@ -10,20 +10,24 @@
 // by arithmetic.  The design therefore puts every gather in flight early and keeps
 // the per-key work on tensor cores:
 //  * the cluster's CTAs (up to 16) split the attended keys of (b, g); inside a CTA
-//    each warp owns every fourth 16-key sub-tile, gathers it (16-byte cp.async, a
-//    token's row for head g is 2*D contiguous bytes) into its own shared-memory ring
-//    with kNBuf sub-tiles in flight, and keeps its own online softmax; the key
-//    positions of a CTA's range are read in one round (the selected slots are read
-//    before the row's sink count is known, on the assumption that it is full);
+//    each of the four warps owns every fourth 16-key sub-tile, gathers it (16-byte
+//    cp.async, a token's row for head g is 2*D contiguous bytes) into its own
+//    shared-memory ring with up to three sub-tiles in flight, and keeps its own online
+//    softmax; the key positions of a CTA's range, the row's counts and the query are
+//    read in one round (the selected slots are read before the row's sink count is
+//    known, on the assumption that it is full).  Rings deeper than that would hold a
+//    range in one round but raise shared memory past two CTAs per SM, and then fewer
+//    16-CTA clusters than the 1M workload's eight KV heads fit the GPU at once;
 //  * S = Q K^T and O += P V are mma.sync m16n8k16 (bf16 in, fp32 accumulate): the
 //    G*T_q query rows (at most 16) of the KV head are the M = 16 rows, keys and head
 //    dimensions the N and K sides; P goes from the S accumulators straight into the A
 //    operand of the P V product;
 //  * the running max is exact (the row's largest probability is exactly 1) and the
 //    row sum adds the same bf16-rounded probabilities that enter P V;
-//  * at the end the four warps of a CTA merge in shared memory and the CTAs of the
-//    cluster merge through distributed shared memory (log-sum-exp weights); nothing
-//    goes through HBM but the K/V rows, the query and the output.
+//  * at the end the warps of a CTA merge in shared memory (over the drained rings) and
+//    the CTAs of the cluster merge through distributed shared memory (log-sum-exp
+//    weights; eight threads per output read their CTAs' partials in one round);
+//    nothing goes through HBM but the K/V rows, the query and the output.
 #include <cooperative_groups.h>
 #include <math.h>
 
@@ -35,27 +39,39 @@
 namespace dsa {
 namespace {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;   // x three ring slots x 8 KiB (d = 128): two CTAs per SM
 constexpr int kThreads = kWarps * 32;
 constexpr int kST = 16;      // keys per warp sub-tile
-constexpr int kNBuf = 3;     // sub-tiles in flight per warp (two CTAs fit an SM)
+constexpr int kMaxBuf = 3;   // sub-tiles in flight per warp, at most
+constexpr int kTPE = 8;      // threads per output in the cluster merge (C <= 2 * kTPE)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
 // Shared rows are D bf16 with the 16-byte pieces of key row k stored at piece index
 // c ^ (k & 7): the eight rows an ldmatrix reads at one piece index hit eight
-// different bank groups.
+// different bank groups.  The warp and CTA partials reuse the rings once every gather
+// has landed.
 template <int D>
 struct MmaSmem {
   static constexpr int kRow = D;                // bf16 per shared row
   static constexpr int kSlot = 2 * kST * kRow;  // K rows then V rows of one sub-tile
-  static size_t bytes(int kps, int R) {
-    size_t o = static_cast<size_t>(kWarps) * kNBuf * kSlot * 2;   // the warps' rings
-    o += static_cast<size_t>(kps) * 4;                             // key positions
-    o += static_cast<size_t>(kWarps + 1) * R * (D + 2) * 4;        // warp and CTA partials
-    return o;
+  __host__ __device__ static size_t ring_bytes(int nbuf) { return static_cast<size_t>(kWarps) * nbuf * kSlot * 2; }
+  __host__ __device__ static size_t part_bytes(int R) {             // warp partials, CTA partial, merge weights
+    return (static_cast<size_t>(kWarps + 1) * R * (D + 2) + static_cast<size_t>(kWarps) * R) * 4;
+  }
+  __host__ __device__ static size_t rings_or_parts(int nbuf, int R) {
+    return ring_bytes(nbuf) > part_bytes(R) ? ring_bytes(nbuf) : part_bytes(R);
+  }
+  static size_t bytes(int kps, int R, int nbuf) {
+    return rings_or_parts(nbuf, R) + static_cast<size_t>(kps) * 4;   // + key positions
   }
 };
+
+// ring slots a warp needs for a range of kps keys (every sub-tile in flight if it fits)
+inline int ring_slots(int kps) {
+  const int per_warp = ((kps + kST - 1) / kST + kWarps - 1) / kWarps;
+  return per_warp < 1 ? 1 : (per_warp > kMaxBuf ? kMaxBuf : per_warp);
+}
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_addr(smem_dst)),
@@ -72,7 +88,7 @@ __device__ __forceinline__ float bf16r(float x) {   // x rounded to bf16 (neares
   return __uint_as_float(static_cast<uint32_t>(f32_to_bf16(x)) << 16);
 }
 
-template <int D>
+template <int D, int NBUF>
 __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   namespace cg = cooperative_groups;
   using SM = MmaSmem<D>;
@@ -83,8 +99,8 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   const int G = a.H_q / a.H_kv;
   const int R = G * a.T_q;     // <= 16
   uint16_t *ring = reinterpret_cast<uint16_t *>(smem);
-  int *s_pos = reinterpret_cast<int *>(ring + kWarps * kNBuf * SM::kSlot);
-  float *s_part = reinterpret_cast<float *>(s_pos + a.keys_per_split);   // [kWarps + 1][R][D + 2]
+  float *s_part = reinterpret_cast<float *>(smem);   // over the drained rings
+  int *s_pos = reinterpret_cast<int *>(smem + SM::rings_or_parts(NBUF, R));
 
   grid_dep_wait();
   cg::cluster_group cluster = cg::this_cluster();
@@ -93,6 +109,24 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   const int g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int gq = lane >> 2, tq = lane & 3;
+  // the query rows as A fragments (row r = t * G + j of head g * G + j; rows >= R zero),
+  // loaded in the same round as the key positions below
+  uint32_t qa[KS][4];
+  {
+    const uint16_t *q = static_cast<const uint16_t *>(a.q);
+    auto qpair = [&](int r, int d) -> uint32_t {
+      if (r >= R) return 0u;
+      const int t = r / G, h = g * G + (r - t * G);
+      return *reinterpret_cast<const uint32_t *>(q + ((static_cast<size_t>(b) * a.T_q + t) * a.H_q + h) * D + d);
+    };
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      qa[ks][0] = qpair(gq, ks * 16 + 2 * tq);
+      qa[ks][1] = qpair(gq + 8, ks * 16 + 2 * tq);
+      qa[ks][2] = qpair(gq, ks * 16 + 8 + 2 * tq);
+      qa[ks][3] = qpair(gq + 8, ks * 16 + 8 + 2 * tq);
+    }
+  }
   const int32_t *sel = a.sel_idx + static_cast<size_t>(b) * a.max_sel;
   const int k_begin = rank * a.keys_per_split;
   // the selected positions this range would hold if every sink slot were filled, read
@@ -113,7 +147,6 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   const int a_len = n_s + cnt + n_w;
   const int k_end = min(a_len, k_begin + a.keys_per_split);
   const int n_sub = k_end > k_begin ? (k_end - k_begin + kST - 1) / kST : 0;
-  const uint16_t *q = static_cast<const uint16_t *>(a.q);
   const uint16_t *kbase = static_cast<const uint16_t *>(a.k) +
                           static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D;
   const uint16_t *vbase = static_cast<const uint16_t *>(a.v) +
@@ -142,25 +175,9 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
     const int xs = k_begin + i - a.n_sink;
     s_pos[i] = position(i, xs >= 0 && xs < a.max_sel ? sel[xs] : -1);
   }
-  // the query rows as A fragments (row r = t * G + j of head g * G + j; rows >= R zero)
-  uint32_t qa[KS][4];
-  {
-    auto qpair = [&](int r, int d) -> uint32_t {
-      if (r >= R) return 0u;
-      const int t = r / G, h = g * G + (r - t * G);
-      return *reinterpret_cast<const uint32_t *>(q + ((static_cast<size_t>(b) * a.T_q + t) * a.H_q + h) * D + d);
-    };
-#pragma unroll
-    for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = qpair(gq, ks * 16 + 2 * tq);
-      qa[ks][1] = qpair(gq + 8, ks * 16 + 2 * tq);
-      qa[ks][2] = qpair(gq, ks * 16 + 8 + 2 * tq);
-      qa[ks][3] = qpair(gq + 8, ks * 16 + 8 + 2 * tq);
-    }
-  }
   __syncthreads();
 
-  uint16_t *wring = ring + warp * kNBuf * SM::kSlot;
+  uint16_t *wring = ring + warp * NBUF * SM::kSlot;
   // sub-tile j of the CTA range -> ring slot `slot` (one commit group per call)
   auto issue = [&](int j, int slot) {
     if (j < n_sub) {
@@ -191,10 +208,10 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;   // rows gq and gq + 8
 
 #pragma unroll
-  for (int s = 0; s < kNBuf; ++s) issue(warp + s * kWarps, s);
+  for (int s = 0; s < NBUF; ++s) issue(warp + s * kWarps, s);
   for (int it = 0, j = warp; j < n_sub; ++it, j += kWarps) {
-    const int slot = it % kNBuf;
-    asm volatile("cp.async.wait_group %0;\n" ::"n"(kNBuf - 1) : "memory");
+    const int slot = it % NBUF;
+    asm volatile("cp.async.wait_group %0;\n" ::"n"(NBUF - 1) : "memory");
     __syncwarp();
     const uint16_t *sk = wring + slot * SM::kSlot;
     const uint16_t *sv = sk + kST * SM::kRow;
@@ -275,11 +292,12 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
       }
     }
     __syncwarp();
-    issue(j + kNBuf * kWarps, slot);
+    issue(j + NBUF * kWarps, slot);
   }
   asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+  __syncthreads();   // every ring drained: the partials below overwrite them
 
-  // this warp's partial for the rows it holds
+  // this warp's partial for the rows it holds: [warp][R][D + 2] = (acc, m, l)
   {
     float *wp = s_part + static_cast<size_t>(warp) * R * (D + 2);
 #pragma unroll
@@ -306,51 +324,82 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
     }
   }
   __syncthreads();
-  // the CTA's partial from its four warps
+  // the CTA's partial from its warps: per row the max and the warps' weights once, then
+  // every element as a weighted sum
   float *cp = s_part + static_cast<size_t>(kWarps) * R * (D + 2);
-  for (int e = tid; e < R * (D + 1); e += kThreads) {
-    const int r = e / (D + 1), d = e - r * (D + 1);   // d == D: the row's (m, l)
+  float *s_wgt = cp + static_cast<size_t>(R) * (D + 2);   // [kWarps][R]
+  if (tid < R) {
+    const int r = tid;
     float M = -INFINITY;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) M = fmaxf(M, s_part[(w * R + r) * (D + 2) + D]);
-    float acc = 0.f;
+    float L = 0.f;
 #pragma unroll
     for (int w = 0; w < kWarps; ++w) {
-      const float *wr = s_part + (w * R + r) * (D + 2);
-      const float wgt = (wr[D] == -INFINITY) ? 0.f : exp2f(wr[D] - M);
-      acc = fmaf(d < D ? wr[d] : wr[D + 1], wgt, acc);
+      const float m = s_part[(w * R + r) * (D + 2) + D];
+      const float wgt = (m == -INFINITY) ? 0.f : exp2f(m - M);
+      s_wgt[w * R + r] = wgt;
+      L = fmaf(s_part[(w * R + r) * (D + 2) + D + 1], wgt, L);
     }
-    if (d < D) {
-      cp[r * (D + 2) + d] = acc;
-    } else {
-      cp[r * (D + 2) + D] = M;
-      cp[r * (D + 2) + D + 1] = acc;
-    }
+    cp[r * (D + 2) + D] = M;
+    cp[r * (D + 2) + D + 1] = L;
+  }
+  __syncthreads();
+  for (int e = tid; e < R * D; e += kThreads) {
+    const int r = e / D, d = e - r * D;
+    float acc = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) acc = fmaf(s_part[(w * R + r) * (D + 2) + d], s_wgt[w * R + r], acc);
+    cp[r * (D + 2) + d] = acc;
   }
   cluster.sync();
-  // merge across the cluster: the CTAs share the R*D outputs
+  // merge across the cluster: the CTAs share the R*D outputs; kTPE threads per output,
+  // each reading the partials of CTAs part and part + kTPE, so every remote load of an
+  // output is issued in one round
   const int E = R * D;
   const int per = (E + C - 1) / C;
-  const int e_end = min(E, (rank + 1) * per);
-  for (int e = rank * per + tid; e < e_end; e += kThreads) {
-    const int r = e / D, d = e - r * D;
+  const int e_beg = rank * per, e_end = min(E, e_beg + per);
+  const int part = tid & (kTPE - 1);
+  for (int base = e_beg; base < e_end; base += kThreads / kTPE) {   // uniform trip count
+    const int e = base + tid / kTPE;
+    const bool valid = e < e_end;
+    const int r = valid ? e / D : 0, d = valid ? e - r * D : 0;
     const float *pr = cp + r * (D + 2);
-    float M = -INFINITY;
-    for (int c = 0; c < C; ++c) M = fmaxf(M, *cluster.map_shared_rank(pr + D, c));
-    float Ls = 0.f, ov = 0.f;
-    if (M != -INFINITY) {
-      for (int c = 0; c < C; ++c) {
-        const float m = *cluster.map_shared_rank(pr + D, c);
-        if (m == -INFINITY) continue;
-        const float wgt = exp2f(m - M);
-        Ls = fmaf(*cluster.map_shared_rank(pr + D + 1, c), wgt, Ls);
-        ov = fmaf(*cluster.map_shared_rank(pr + d, c), wgt, ov);
+    float mc[2], lc[2], oc[2];
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int c = part + u * kTPE;
+      mc[u] = -INFINITY;
+      lc[u] = oc[u] = 0.f;
+      if (valid && c < C) {
+        mc[u] = *cluster.map_shared_rank(pr + D, c);
+        lc[u] = *cluster.map_shared_rank(pr + D + 1, c);
+        oc[u] = *cluster.map_shared_rank(pr + d, c);
       }
     }
-    const int t = r / G, h = g * G + (r - t * G);
-    const size_t row = (static_cast<size_t>(b) * a.T_q + t) * a.H_q + h;
-    static_cast<uint16_t *>(a.out)[row * D + d] = f32_to_bf16(Ls > 0.f ? ov / Ls : 0.f);
-    if (a.lse && d == 0) a.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    float M = fmaxf(mc[0], mc[1]);
+#pragma unroll
+    for (int x = 1; x < kTPE; x <<= 1) M = fmaxf(M, __shfl_xor_sync(kFull, M, x));
+    float Ls = 0.f, ov = 0.f;
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      if (mc[u] != -INFINITY) {
+        const float wgt = exp2f(mc[u] - M);
+        Ls = fmaf(lc[u], wgt, Ls);
+        ov = fmaf(oc[u], wgt, ov);
+      }
+    }
+#pragma unroll
+    for (int x = 1; x < kTPE; x <<= 1) {
+      Ls += __shfl_xor_sync(kFull, Ls, x);
+      ov += __shfl_xor_sync(kFull, ov, x);
+    }
+    if (valid && part == 0) {
+      const int t = r / G, h = g * G + (r - t * G);
+      const size_t row = (static_cast<size_t>(b) * a.T_q + t) * a.H_q + h;
+      static_cast<uint16_t *>(a.out)[row * D + d] = f32_to_bf16(Ls > 0.f ? ov / Ls : 0.f);
+      if (a.lse && d == 0) a.lse[row] = Ls > 0.f ? (M + log2f(Ls)) * kLn2 : -INFINITY;
+    }
   }
   cluster.sync();   // keep this CTA's shared memory until every reader is done
 }
@@ -360,10 +409,13 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
   DecodeArgs a = a0;
   const int R = (a.H_q / a.H_kv) * a.T_q;
   const int keys = a.n_split * a.keys_per_split;
-  // shared memory sized for the larger range of the 8-CTA fallback below
-  const int kps8 = ((keys / 8 + kST - 1) / kST) * kST;
-  const size_t smem = MmaSmem<D>::bytes(kps8 > a.keys_per_split ? kps8 : a.keys_per_split, R);
-  auto kern = decode_mma_kernel<D>;
+  auto kernel_for = [](int nbuf) {
+    return nbuf == 1 ? decode_mma_kernel<D, 1> : nbuf == 2 ? decode_mma_kernel<D, 2>
+                                                           : decode_mma_kernel<D, 3>;
+  };
+  int nbuf = ring_slots(a.keys_per_split);
+  auto kern = kernel_for(nbuf);
+  size_t smem = MmaSmem<D>::bytes(a.keys_per_split, R, nbuf);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.n_split > 8) {
@@ -391,8 +443,14 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
     if (cudaOccupancyMaxActiveClusters(&n_clusters, kern, &cfg) != cudaSuccess || n_clusters < 1) {
       (void)cudaGetLastError();
       a.n_split = 8;
-      a.keys_per_split = kps8;
+      a.keys_per_split = ((keys / 8 + kST - 1) / kST) * kST;
+      nbuf = ring_slots(a.keys_per_split);
+      kern = kernel_for(nbuf);
+      smem = MmaSmem<D>::bytes(a.keys_per_split, R, nbuf);
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+      if (e != cudaSuccess) return e;
       cfg.gridDim.x = 8;
+      cfg.dynamicSmemBytes = smem;
       attr[0].val.clusterDim.x = 8;
     }
   }
