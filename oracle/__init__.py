@@ -13,10 +13,12 @@ Modules:
            attention over sink + selected + window keys.
   vs    -- MInference vertical-slash estimate, top-k, conversion to the tiled
            block/column format, and sparse causal prefill attention.
+  patterns -- MInference A-shape (static initial blocks + diagonal band) and
+           Block-Sparse (mean-pooled block attention, top-k_b blocks) lists.
   numerics -- exact widening of the stored bit patterns to float64.
 
 Pinning status (what each function is checked against) is listed in the
 module docstrings; the selection heuristic's tie readings are pinned only by
 the written readings of the pages (see the "parity unpinned" notes).
 """
-from . import hip, numerics, vs  # noqa: F401
+from . import hip, numerics, patterns, vs  # noqa: F401
