@@ -522,6 +522,65 @@ def main():
                         "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)",
                         "algorithmic_flops_per_launch": flops}
 
+    # ---------------- other MInference head patterns on the same prefill kernel
+    def time_pattern(build, steps):
+        lists = build()
+        torch.cuda.synchronize()
+        for _ in range(2):
+            build()
+            dsa.sparse_attn_prefill(pq, pk, pv, lists["blk_cnt"], lists["blk_idx"],
+                                    lists["col_cnt"], None, out=pout, lse=plse)
+        ib, at = [], []
+        for _ in range(steps):
+            flush()
+            e0, e1, e2 = ev(), ev(), ev()
+            e0.record()
+            build()
+            e1.record()
+            dsa.sparse_attn_prefill(pq, pk, pv, lists["blk_cnt"], lists["blk_idx"],
+                                    lists["col_cnt"], None, out=pout, lse=plse)
+            e2.record()
+            ib.append((e0, e1))
+            at.append((e1, e2))
+        torch.cuda.synchronize()
+        ib = statistics.mean(a.elapsed_time(b) for a, b in ib)
+        at = statistics.mean(a.elapsed_time(b) for a, b in at)
+        bc = lists["blk_cnt"].cpu().numpy()
+        fl = accounting.prefill_tile_flops(bc, np.zeros_like(bc), pre.D)
+        return {"index_ms": ib, "attention_ms": at, "tiles": int(bc.sum()),
+                "tile_density_vs_causal_dense": float(bc.sum()) / dense_tiles,
+                "tile_flops": fl, "attention_TFLOPs": fl / (at * 1e-3) / 1e12,
+                "attention_tc_frac": fl / (at * 1e-3) / 1e12 / tc_peak}
+
+    n_qb = (pre.S + 63) // 64
+    pat_steps = max(2, min(args.steps, 4))
+    ash = {"blk_cnt": torch.empty(1, pre.H_q, n_qb, dtype=torch.int32, device=dev),
+           "blk_idx": torch.empty(1, pre.H_q, n_qb, 80, dtype=torch.int32, device=dev),
+           "col_cnt": torch.empty(1, pre.H_q, n_qb, dtype=torch.int32, device=dev)}
+    bsl = {"blk_cnt": torch.empty(1, pre.H_q, n_qb, dtype=torch.int32, device=dev),
+           "blk_idx": torch.empty(1, pre.H_q, n_qb, 100, dtype=torch.int32, device=dev),
+           "col_cnt": torch.empty(1, pre.H_q, n_qb, dtype=torch.int32, device=dev)}
+    ws_bs = torch.empty(dsa.block_sparse_index_build_workspace_bytes(pq, pk), dtype=torch.uint8,
+                        device=dev)
+    patterns_line = {
+        "a_shape": dict(time_pattern(lambda: dsa.ashape_index_build(
+            pq, pk, n_global=1024, n_local=4096, out=ash), pat_steps), n_global=1024, n_local=4096),
+        "block_sparse": dict(time_pattern(lambda: dsa.block_sparse_index_build(
+            pq, pk, k_b=100, out=bsl, workspace=ws_bs), pat_steps), k_b=100),
+    }
+    pool_bytes = accounting.block_sparse_pool_bytes(1, pre.S, pre.H_q, pre.H_kv, pre.D)
+    dsa.profile_enable(True)
+    for _ in range(pat_steps):
+        flush()
+        dsa.block_sparse_index_build(pq, pk, k_b=100, out=bsl, workspace=ws_bs)
+    torch.cuda.synchronize()
+    dsa.profile_enable(False)
+    for name, (n, t) in dsa.profile_collect().items():
+        patterns_line["block_sparse"][f"{name}_us"] = 1e3 * t / n
+        if name == "bs_pool":
+            patterns_line["block_sparse"]["bs_pool_GBps"] = pool_bytes / (t / n * 1e-3) / 1e9
+            patterns_line["block_sparse"]["bs_pool_hbm_frac"] = pool_bytes / (t / n * 1e-3) / 1e9 / hbm
+
     # ---------------- end to end through the public API with host buffers
     h_q = torch.empty(q.shape, dtype=q.dtype, pin_memory=True)
     h_q.copy_(q)
@@ -613,6 +672,9 @@ def main():
             "chunks_per_stage": stage_chunks,
             "attended_keys": attended,
         },
+        # the same prefill kernel over MInference A-shape (1024 initial + 4096 local tokens)
+        # and Block-Sparse (k_b = 100) lists built on the GPU, same inputs
+        "prefill_patterns": patterns_line,
         # mask caching (InfiniteHiP section 3.4): the same step with stage i recomputed only
         # when step % n_refresh[i] == 0, averaged over whole refresh periods
         "decode_cached": cached,

@@ -8,6 +8,9 @@ has not been built (``__graft_entry__.build()``).
 """
 from .binding import (  # noqa: F401
     DsaError,
+    ashape_index_build,
+    block_sparse_index_build,
+    block_sparse_index_build_workspace_bytes,
     device_error,
     HipConfig,
     hip_max_chunks,

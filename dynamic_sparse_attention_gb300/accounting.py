@@ -76,6 +76,12 @@ def vs_index_bytes(B, S, H_q, H_kv, D, n_vertical, elem=2) -> float:
     return float(2 * B * S * H_kv * D * elem + 2 * B * 64 * H_q * D * elem)
 
 
+def block_sparse_pool_bytes(B, S, H_q, H_kv, D, elem=2) -> float:
+    """Block-Sparse pooling: every q and k row read once, fp32 pooled blocks written."""
+    nb = -(-S // 64)
+    return float(B) * (S * (H_q + H_kv) * D * elem + nb * (H_q + H_kv) * D * 4)
+
+
 def causal_dense_tiles(S: int) -> int:
     n = math.ceil(S / 64)
     return n * (n + 1) // 2

@@ -51,6 +51,10 @@ class VsDebug(ctypes.Structure):
     _fields_ = [("vsum", _vp), ("ssum", _vp)]
 
 
+class BsDebug(ctypes.Structure):
+    _fields_ = [("q_pool", _vp), ("k_pool", _vp), ("scores", _vp)]
+
+
 class KernelStat(ctypes.Structure):
     _fields_ = [("name", ctypes.c_char_p), ("launches", _c_int), ("total_ms", ctypes.c_double)]
 
@@ -80,6 +84,10 @@ _SIGNATURES = {
     "vs_index_build_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
     "vs_index_build": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp,
                                 ctypes.c_size_t, _vp]),
+    "ashape_index_build": (_c_int, [_vp, _c_int, _c_int, _c_int, _c_int, _vp, _vp, _vp, _vp]),
+    "block_sparse_index_build_workspace": (_c_int, [_vp, _c_int, ctypes.POINTER(ctypes.c_size_t)]),
+    "block_sparse_index_build": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
+                                          _vp, _vp, ctypes.c_size_t, _vp]),
     "sparse_attn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                      _vp, ctypes.c_float, _vp, _vp, _vp]),
     "sparse_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
@@ -440,9 +448,80 @@ def vs_index_build(q, k, *, last_q: int = 64, n_vertical: int, n_slash: int, blo
     return out
 
 
+def _block_lists(B, H_q, nq, max_blk, dev, out):
+    if out is None:
+        out = {
+            "blk_cnt": torch.empty(B, H_q, nq, dtype=torch.int32, device=dev),
+            "blk_idx": torch.empty(B, H_q, nq, max(max_blk, 1), dtype=torch.int32, device=dev),
+            "col_cnt": torch.empty(B, H_q, nq, dtype=torch.int32, device=dev),
+        }
+    out.setdefault("col_idx", None)
+    return out
+
+
+def ashape_index_build(q, k, *, n_global: int, n_local: int, block: int = 64, max_blk=None,
+                       out: dict | None = None, stream=None):
+    """A-shape lists (initial blocks + a band ending at the diagonal); q and k give the
+    shape only.  Returns a dict with blk_cnt, blk_idx, col_cnt (all 0), col_idx None."""
+    lib = load()
+    shape = prefill_shape(q, k)
+    nq = (shape.S + block - 1) // block
+    if max_blk is None:
+        max_blk = min(nq, n_global // block + n_local // block)
+    out = _block_lists(shape.B, shape.H_q, nq, max_blk, q.device, out)
+    _need_cuda(out["blk_cnt"], out["blk_idx"], out["col_cnt"])
+    st = lib.ashape_index_build(ctypes.byref(shape), block, n_global, n_local,
+                                out["blk_idx"].shape[-1], _ptr(out["blk_cnt"]),
+                                _ptr(out["blk_idx"]), _ptr(out["col_cnt"]), _stream(stream))
+    _check("ashape_index_build", st)
+    return out
+
+
+def block_sparse_index_build_workspace_bytes(q, k, block: int = 64) -> int:
+    lib = load()
+    n = ctypes.c_size_t()
+    shape = prefill_shape(q, k)
+    _check("block_sparse_index_build_workspace",
+           lib.block_sparse_index_build_workspace(ctypes.byref(shape), block, ctypes.byref(n)))
+    return n.value
+
+
+def block_sparse_index_build(q, k, *, k_b: int, block: int = 64, max_blk=None,
+                             debug: bool = False, out: dict | None = None, workspace=None,
+                             stream=None):
+    """Block-Sparse lists (mean-pooled block attention, top-k_b key blocks per query
+    block).  Returns a dict with blk_cnt, blk_idx, col_cnt (all 0), col_idx None and,
+    with debug, the pooled blocks and the block logits."""
+    lib = load()
+    _need_cuda(q, k)
+    shape = prefill_shape(q, k)
+    B, S, H_q = shape.B, shape.S, shape.H_q
+    nq = (S + block - 1) // block
+    if max_blk is None:
+        max_blk = min(k_b, nq)
+    out = _block_lists(B, H_q, nq, max_blk, q.device, out)
+    dbg = None
+    if debug:
+        dev = q.device
+        out["q_pool"] = torch.empty(B, H_q, nq, shape.D, dtype=torch.float32, device=dev)
+        out["k_pool"] = torch.empty(B, shape.H_kv, nq, shape.D, dtype=torch.float32, device=dev)
+        out["scores"] = torch.full((B, H_q, nq, nq), float("nan"), dtype=torch.float32, device=dev)
+        dbg = BsDebug(out["q_pool"].data_ptr(), out["k_pool"].data_ptr(),
+                      out["scores"].data_ptr())
+    ws = _workspace(block_sparse_index_build_workspace_bytes(q, k, block), q.device, workspace)
+    st = lib.block_sparse_index_build(_ptr(q), _ptr(k), ctypes.byref(shape), block, k_b,
+                                      out["blk_idx"].shape[-1], _ptr(out["blk_cnt"]),
+                                      _ptr(out["blk_idx"]), _ptr(out["col_cnt"]),
+                                      ctypes.byref(dbg) if dbg else None, _ptr(ws),
+                                      ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check("block_sparse_index_build", st)
+    return out
+
+
 def sparse_attn_prefill(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx, *, scale=None,
                         block: int = 64, out=None, lse=None, want_lse: bool = True, stream=None):
-    """Causal attention over the listed tiles and columns; returns (out, lse or None)."""
+    """Causal attention over the listed tiles and columns (col_idx None: no columns);
+    returns (out, lse or None)."""
     lib = load()
     _need_cuda(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx)
     shape = prefill_shape(q, k)
@@ -453,7 +532,8 @@ def sparse_attn_prefill(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx, *, scale=No
     if lse is None and want_lse:
         lse = torch.empty(shape.B, shape.H_q, shape.S, dtype=torch.float32, device=q.device)
     st = lib.sparse_attn_prefill(_ptr(q), _ptr(k), _ptr(v), ctypes.byref(shape), block,
-                                 blk_idx.shape[-1], col_idx.shape[-1], _ptr(blk_cnt),
+                                 blk_idx.shape[-1], 0 if col_idx is None else col_idx.shape[-1],
+                                 _ptr(blk_cnt),
                                  _ptr(blk_idx), _ptr(col_cnt), _ptr(col_idx),
                                  ctypes.c_float(scale), _ptr(out), _ptr(lse), _stream(stream))
     _check("sparse_attn_prefill", st)

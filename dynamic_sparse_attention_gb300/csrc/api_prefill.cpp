@@ -1,4 +1,6 @@
-// C-ABI entry points of the prefill half: vs_index_build and sparse_attn_prefill.
+// C-ABI entry points of the prefill half: vs_index_build, ashape_index_build,
+// block_sparse_index_build and sparse_attn_prefill.
+#include <algorithm>
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
@@ -63,6 +65,21 @@ VsWs vs_layout(const dsa_prefill_shape *s, void *base) {
   w.vsum = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * s->S);
   w.ssum = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * s->S);
   w.slash_part = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * w.n_ktile * kDiagPerTile);
+  w.bytes = cv.bytes();
+  return w;
+}
+
+struct BsWs {
+  float *q_pool, *k_pool;
+  size_t bytes;
+};
+
+BsWs bs_layout(const dsa_prefill_shape *s, void *base) {
+  BsWs w{};
+  Carve cv(base);
+  const size_t nb = (s->S + kBlock - 1) / kBlock;
+  w.q_pool = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * nb * s->D);
+  w.k_pool = cv.take<float>(static_cast<size_t>(s->B) * s->H_kv * nb * s->D);
   w.bytes = cv.bytes();
   return w;
 }
@@ -178,6 +195,98 @@ int sparse_attn_prefill(const void *q, const void *k, const void *v,
   cudaError_t e = use_mma ? launch_prefill_mma(a, static_cast<cudaStream_t>(stream))
                           : launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_prefill launch");
+  return DSA_OK;
+}
+
+int ashape_index_build(const dsa_prefill_shape *shape, int block, int n_global, int n_local,
+                       int max_blk, int32_t *blk_cnt, int32_t *blk_idx, int32_t *col_cnt,
+                       void *stream) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
+  if (n_global < 0 || n_local < 0 || n_global % kBlock || n_local % kBlock)
+    return fail(DSA_ERR_INVALID_ARG, "n_global=%d / n_local=%d must be non-negative multiples of 64",
+                n_global, n_local);
+  const long n_qblk = (shape->S + kBlock - 1) / kBlock;
+  const long need = std::min(n_qblk, static_cast<long>(n_global / kBlock) + n_local / kBlock);
+  if (max_blk < need)
+    return fail(DSA_ERR_INVALID_ARG, "max_blk=%d < %ld blocks per query block", max_blk, need);
+  if (!aligned(blk_cnt, 4) || !aligned(col_cnt, 4) || (max_blk > 0 && !aligned(blk_idx, 4)))
+    return fail(DSA_ERR_ALIGNMENT, "list arrays must be non-NULL and 4-byte aligned");
+  AshapeArgs a{};
+  a.BH = shape->B * shape->H_q;
+  a.n_qblk = static_cast<int>(n_qblk);
+  a.max_blk = max_blk;
+  a.n_global_blk = n_global / kBlock;
+  a.n_local_blk = n_local / kBlock;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  cudaError_t e = launch_ashape(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "ashape_index_build launch");
+  return DSA_OK;
+}
+
+int block_sparse_index_build_workspace(const dsa_prefill_shape *shape, int block, size_t *bytes) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
+  if (!bytes) return fail(DSA_ERR_ALIGNMENT, "bytes is NULL");
+  *bytes = bs_layout(shape, nullptr).bytes;
+  return DSA_OK;
+}
+
+int block_sparse_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
+                             int block, int k_b, int max_blk, int32_t *blk_cnt, int32_t *blk_idx,
+                             int32_t *col_cnt, const dsa_bs_debug *dbg, void *ws, size_t ws_bytes,
+                             void *stream) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
+  const int nb = (shape->S + kBlock - 1) / kBlock;
+  if (k_b < 0) return fail(DSA_ERR_INVALID_ARG, "k_b=%d < 0", k_b);
+  if (max_blk < std::min(k_b, nb))
+    return fail(DSA_ERR_INVALID_ARG, "max_blk=%d < min(k_b=%d, n_qblk=%d)", max_blk, k_b, nb);
+  if (bs_rows_per_cta(nb, shape->D) < 1)
+    return fail(DSA_ERR_UNSUPPORTED, "S=%d: a row of %d block scores exceeds shared memory",
+                shape->S, nb);
+  if (!aligned(q, 16) || !aligned(k, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q and k must be non-NULL and 16-byte aligned");
+  if (!aligned(blk_cnt, 4) || !aligned(col_cnt, 4) || (max_blk > 0 && !aligned(blk_idx, 4)))
+    return fail(DSA_ERR_ALIGNMENT, "list arrays must be non-NULL and 4-byte aligned");
+  if (dbg && ((dbg->q_pool && !aligned(dbg->q_pool, 16)) || (dbg->k_pool && !aligned(dbg->k_pool, 16)) ||
+              (dbg->scores && !aligned(dbg->scores, 4))))
+    return fail(DSA_ERR_ALIGNMENT, "debug arrays must be 16-byte (pools) / 4-byte aligned");
+  const size_t need = bs_layout(shape, nullptr).bytes;
+  if (ws_bytes < need || !aligned(ws, 16))
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu", need,
+                ws_bytes);
+  const BsWs w = bs_layout(shape, ws);
+  BsArgs a{};
+  a.q = q;
+  a.k = k;
+  a.B = shape->B;
+  a.S = shape->S;
+  a.H_q = shape->H_q;
+  a.H_kv = shape->H_kv;
+  a.D = shape->D;
+  a.nb = nb;
+  a.k_b = k_b;
+  a.max_blk = max_blk;
+  a.scale = 1.f / std::sqrt(static_cast<float>(shape->D));
+  a.q_pool = w.q_pool;
+  a.k_pool = w.k_pool;
+  a.dbg_q_pool = dbg ? dbg->q_pool : nullptr;
+  a.dbg_k_pool = dbg ? dbg->k_pool : nullptr;
+  a.dbg_scores = dbg ? dbg->scores : nullptr;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  cudaError_t e = launch_block_sparse(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "block_sparse_index_build launch");
   return DSA_OK;
 }
 

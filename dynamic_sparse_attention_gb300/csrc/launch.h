@@ -132,4 +132,27 @@ cudaError_t launch_prefill_mma(const PrefillArgs &a, cudaStream_t s);
 bool prefill_tc_supported(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 
+// MInference A-shape block lists (static: the initial blocks plus a band ending at the
+// diagonal block).
+struct AshapeArgs {
+  int BH, n_qblk, max_blk;
+  int n_global_blk, n_local_blk;
+  int32_t *blk_cnt, *blk_idx, *col_cnt;
+};
+cudaError_t launch_ashape(const AshapeArgs &a, cudaStream_t s);
+
+// MInference Block-Sparse estimate: mean-pooled blocks, top-k_b key blocks per row.
+struct BsArgs {
+  const void *q, *k;
+  int B, S, H_q, H_kv, D;
+  int nb, k_b, max_blk;
+  float scale;
+  float *q_pool, *k_pool;                          // scratch [B, H_q|H_kv, nb, D]
+  float *dbg_q_pool, *dbg_k_pool, *dbg_scores;     // optional copies / [B, H_q, nb, nb]
+  int32_t *blk_cnt, *blk_idx, *col_cnt;
+};
+cudaError_t launch_block_sparse(const BsArgs &a, cudaStream_t s);
+// query blocks per CTA of the scoring kernel (0: nb too large for shared memory)
+int bs_rows_per_cta(int nb, int D);
+
 }  // namespace dsa

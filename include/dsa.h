@@ -7,6 +7,9 @@
  *                                   sink + selected + window keys, with a merge
  *   prefill: vs_index_build      -- MInference vertical-slash estimate, top-k and
  *                                   conversion to per-query-block tile/column lists
+ *            ashape_index_build  -- MInference A-shape lists (initial blocks + band)
+ *            block_sparse_index_build -- MInference Block-Sparse estimate (mean-pooled
+ *                                   blocks, top-k_b key blocks per query block)
  *            sparse_attn_prefill -- causal attention over those 64x64 tiles and
  *                                   gathered columns
  *
@@ -227,6 +230,54 @@ int vs_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
                    const dsa_vs_cfg *cfg, int32_t *vertical, int32_t *slash, int32_t *blk_cnt,
                    int32_t *blk_idx, int32_t *col_cnt, int32_t *col_idx,
                    const dsa_vs_debug *dbg, void *ws, size_t ws_bytes, void *stream);
+
+/* ashape_index_build -- MInference A-shape lists for every (b, query head): query
+ * block m attends the key blocks j <= m with j < n_global/64 (the initial tokens) or
+ * m - j < n_local/64 (a band of blocks ending at the diagonal block), rows causal
+ * inside the diagonal block.  Source: MInference summary, "The Three Sparse Patterns"
+ * (A-Shape Pattern) and "Sparse GPU Kernel Implementations (Appendix C.4)" (A-Shape
+ * Kernel).  The lists depend on the shape only (q and k are not read).
+ *   n_global, n_local  token counts, non-negative multiples of `block` (64 only)
+ *   blk_cnt [B, H_q, n_qblk], blk_idx [B, H_q, n_qblk, max_blk] ascending key blocks,
+ *   col_cnt [B, H_q, n_qblk] all 0 (call sparse_attn_prefill with max_col = 0)
+ * max_blk below min(n_qblk, n_global/64 + n_local/64) is INVALID_ARG.  Unused tails of
+ * blk_idx rows are left untouched. */
+int ashape_index_build(const dsa_prefill_shape *shape, int block, int n_global, int n_local,
+                       int max_blk, int32_t *blk_cnt, int32_t *blk_idx, int32_t *col_cnt,
+                       void *stream);
+
+/* Optional Block-Sparse intermediates for inspection (each may be NULL):
+ *   q_pool [B, H_q, n_qblk, D], k_pool [B, H_kv, n_qblk, D] fp32 mean-pooled blocks;
+ *   scores [B, H_q, n_qblk, n_qblk] fp32 scaled block logits q~ . k~ / sqrt(D), written
+ *   for key blocks j <= m only (small S: n_qblk^2 floats per head). */
+typedef struct {
+  float *q_pool;
+  float *k_pool;
+  float *scores;
+} dsa_bs_debug;
+
+int block_sparse_index_build_workspace(const dsa_prefill_shape *shape, int block,
+                                       size_t *bytes);
+
+/* block_sparse_index_build -- MInference Block-Sparse lists for every (b, query head).
+ * Source: MInference summary, "Online Dynamic Index Estimation: Block-Sparse Heads
+ * (Algorithm 3)", steps 1-4:
+ *   q~ = MeanPooling(q, 64) per query head, k~ = MeanPooling(k, 64) per KV head (a
+ *   ragged last block averages the tokens it has);
+ *   A~ = softmax(q~ k~^T / sqrt(D) + block-causal mask), key blocks after the query
+ *   block masked (the diagonal block stays);
+ *   query block m keeps the min(k_b, m + 1) largest entries of its row (ties -> smaller
+ *   block index), ascending.  Softmax is monotone along a row, so the kernels rank the
+ *   fp32 logits; query head h uses KV head h / (H_q / H_kv).
+ *   blk_cnt / blk_idx [B, H_q, n_qblk(, max_blk)], col_cnt all 0 (max_col = 0 in
+ *   sparse_attn_prefill).
+ * max_blk below min(k_b, n_qblk) is INVALID_ARG; S whose n_qblk block scores do not
+ * fit one CTA's shared memory (S above about 2.08M at D = 128) is UNSUPPORTED.  dbg may be
+ * NULL. */
+int block_sparse_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
+                             int block, int k_b, int max_blk, int32_t *blk_cnt, int32_t *blk_idx,
+                             int32_t *col_cnt, const dsa_bs_debug *dbg, void *ws, size_t ws_bytes,
+                             void *stream);
 
 /* sparse_attn_prefill -- causal attention of each query block over its listed
  * 64x64 key tiles, then its listed columns gathered 64 at a time, with one

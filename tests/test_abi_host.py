@@ -141,3 +141,34 @@ def test_refresh_mask_helper():
     assert binding.refresh_mask(48, (96, 24, 8, 8)) == 0b1110
     with pytest.raises(ValueError):
         binding.refresh_mask(3, (4, 0))
+
+
+def _pshape(**kw):
+    d = dict(B=1, S=4096, H_q=8, H_kv=2, D=128)
+    d.update(kw)
+    return binding.PrefillShape(**d)
+
+
+def test_pattern_builders_validate_arguments(lib):
+    s = _pshape()
+    buf = (ctypes.c_char * 64)()
+    ok = ctypes.c_void_p(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 16))
+    # A-shape: token counts must be multiples of 64, max_blk must hold a row
+    assert lib.ashape_index_build(ctypes.byref(s), 64, 100, 256, 64, ok, ok, ok, None) == -1
+    assert lib.ashape_index_build(ctypes.byref(s), 64, 128, 256, 5, ok, ok, ok, None) == -1
+    assert b"max_blk" in lib.dsa_last_error()
+    assert lib.ashape_index_build(ctypes.byref(s), 32, 128, 256, 64, ok, ok, ok, None) == -2
+    assert lib.ashape_index_build(ctypes.byref(s), 64, 128, 256, 6, None, ok, ok, None) == -4
+    # Block-Sparse: workspace = pooled q and k in fp32
+    n = ctypes.c_size_t()
+    assert lib.block_sparse_index_build_workspace(ctypes.byref(s), 64, ctypes.byref(n)) == 0
+    assert n.value >= 4 * 64 * 128 * (8 + 2)
+    assert lib.block_sparse_index_build(ok, ok, ctypes.byref(s), 64, -1, 10, ok, ok, ok, None, ok,
+                                        ctypes.c_size_t(1 << 30), None) == -1
+    assert lib.block_sparse_index_build(ok, ok, ctypes.byref(s), 64, 100, 50, ok, ok, ok, None, ok,
+                                        ctypes.c_size_t(1 << 30), None) == -1
+    assert lib.block_sparse_index_build(ok, ok, ctypes.byref(s), 64, 10, 10, ok, ok, ok, None, ok,
+                                        ctypes.c_size_t(16), None) == -3
+    big = _pshape(S=4 << 20)
+    assert lib.block_sparse_index_build(ok, ok, ctypes.byref(big), 64, 10, 10, ok, ok, ok, None, ok,
+                                        ctypes.c_size_t(1 << 40), None) == -2
