@@ -7,32 +7,35 @@
 // mask constant taken as exact exclusion.
 //
 // One CTA computes 128 query rows: the two consecutive 64-row query blocks m0 = 2p and
-// m1 = 2p + 1 of one head.  Keys go through the tensor core in 128-key tiles (two
-// consecutive 64-key list blocks): at M = N = K = 128 the MMA runs at its full rate,
-// while 64-key tiles (Q K^T with N = 64, P V with K = 64) reach well under half of it.
-// The CTA walks the 128-key tiles that hold a listed block of either query block
-// (descending, so the running max settles early), then block m0's gathered column tiles
-// (128 columns each), then block m1's; a row masks the 64-key halves its own query
-// block does not list, keys after it (causal) and keys past the sequence end.
-// Warp roles (608 threads):
-//   warp 0     K producer: Q once (TMA), then K tiles (TMA for block tiles, 16-byte
-//              cp.async gathers for column tiles) into a 3-stage ring; writes each
-//              tile's description (kind, key tile, per-half membership, positions);
-//   warp 1     V producer: V tiles into a 2-stage ring (its own walk of the same list);
+// m1 = 2p + 1 of one head.  Keys go through the tensor core in 128-key tiles, each made
+// of two 64-key list blocks: at M = N = K = 128 the MMA runs at its full rate, while
+// 64-key tiles (Q K^T with N = 64, P V with K = 64) reach well under half of it.  The
+// CTA walks the blocks that either query block lists (the union of the two lists),
+// in descending order, and puts each next two of them into a tile (descending, so the
+// running max settles early; any two blocks, so scattered lists fill their tiles),
+// then block m0's gathered column tiles (128 columns each), then block m1's.  A row
+// masks the 64-key halves its own query block does not list, keys after it (causal)
+// and keys past the sequence end.
+// Warp roles (352 threads):
+//   warp 0     K producer: Q once (TMA), then K tiles (two 64-row TMA boxes per 64-wide
+//              head-dim half for block tiles, 16-byte cp.async gathers for column tiles)
+//              into a 3-stage ring; writes each tile's description (kind, the block of
+//              each half, per-half membership, column positions);
+//   warp 1     V producer: V tiles into a 2-stage ring (its own walk of the same lists);
 //   warp 2     MMA issuer (one thread): S_b = Q K^T (M = N = 128, K = D) into one of three
 //              TMEM score buffers (b = tile mod 3), O += P V (A = P read from TMEM,
 //              128 keys).  Q K^T of tile t + 3 is queued right behind P V of tile t, so
 //              the scores of the next two tiles are ready while tile t is in softmax;
-//   warps 3-18 softmax: four threads per query row; warp w reads the TMEM lanes of
-//              quarter w % 4 and one 32-key slice of the tile.  The four slices of a
-//              row combine their maxima through shared memory (a named barrier per lane
-//              quarter); each thread then forms P = exp2(s * scale * log2e - max) with the
-//              exact running max (the row's largest probability is exactly 1, free of
-//              bf16 rounding), keeps a partial row sum, and writes its 16 bf16 pairs over
-//              the first 64 columns of S_b, where the P V MMA reads them.  When the max
-//              grows, each warp brings its quarter of O to the new max once P V of the
-//              previous tile has retired.  The epilogue adds the partial sums,
-//              normalises and stores.
+//   warps 3-10 softmax: two threads per query row; warp w reads the TMEM lanes of
+//              quarter w % 4 and the 64-key half w / 4 of the tile.  The two halves of a
+//              row exchange their maxima through shared memory (an mbarrier per lane
+//              quarter); each thread then forms P = exp2(s * scale * log2e - max) with
+//              the exact running max (the row's largest probability is exactly 1, free
+//              of bf16 rounding), keeps a partial row sum, and writes its bf16 pairs over
+//              the first 64 columns of S_b, where the P V MMA reads them, while the next
+//              tile's scores stream in from TMEM.  When the max grows, each warp brings
+//              its quarter of O to the new max once P V of the previous tile has
+//              retired.  The epilogue adds the partial sums, normalises and stores.
 // Operands: Q and K tiles are K-major with 128-byte swizzle (what TMA writes for a
 // 64-element-wide box); V tiles are the B operand in MN-major form (keys along K).
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work, drains its
@@ -61,7 +64,7 @@ using namespace tc;
 
 constexpr int kRowsQ = 128;        // query rows per CTA
 constexpr int kBlk = 64;           // block size of the tile lists
-constexpr int kKeys = 128;         // keys per MMA tile (two list blocks)
+constexpr int kKeys = 128;         // keys per MMA tile (two list blocks, one per 64-key half)
 constexpr int kKS = 3;             // K ring stages
 constexpr int kVS = 2;             // V ring stages
 constexpr int kSB = 3;             // TMEM score buffers
@@ -79,10 +82,9 @@ static __device__ int g_abort_epoch;         // launch epoch of a launch in whic
 constexpr uint64_t kWaitLimitNs = 500000000ull;
 
 struct TileMeta {
-  int kind;          // 0: 128-key block tile, 1: gathered column tile
-  int n;             // 128-key tile index (kind 0)
+  int kind;          // 0: block tile (two 64-key list blocks), 1: gathered column tile
   int mask;          // bit 2*grp + half: rows of query block m_grp use that 64-key half
-  int ncols;
+  int blk[2];        // the 64-key block held by each half (kind 0)
   int pos[kKeys];    // key positions of a column tile (-1: empty slot)
 };
 static_assert(sizeof(TileMeta) % 16 == 0 && offsetof(TileMeta, pos) % 16 == 0, "int4 reads of pos");
@@ -165,13 +167,10 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, const 
   return ok != 0;
 }
 
-// even bit 2i set <=> block 2i or 2i+1 of the word is listed
-__device__ __forceinline__ uint32_t pair_bits(uint32_t u) { return (u | (u >> 1)) & 0x55555555u; }
-
-// Walk over the 128-key tiles that hold a listed 64-key block of either query block,
-// in descending key order (run by one lane).  Scores near the diagonal are usually the
-// largest of a row, so visiting them first settles the running max early and spares
-// most rescalings of the accumulator.
+// Walk over the blocks either query block lists, in descending key order, two per
+// tile (run by one lane).  Scores near the diagonal are usually the largest of a row,
+// so visiting them first settles the running max early and spares most rescalings of
+// the accumulator.
 struct TileWalk {
   const uint32_t *bm0, *bm1;
   int wi;
@@ -180,21 +179,28 @@ struct TileWalk {
     bm0 = b0;
     bm1 = b1;
     wi = nw - 1;
-    cur = nw > 0 ? pair_bits(bm0[wi] | bm1[wi]) : 0u;
+    cur = nw > 0 ? (bm0[wi] | bm1[wi]) : 0u;
   }
-  // next tile and its membership mask; false once the bitmaps run out
-  __device__ bool next(int &tile, int &mask) {
+  __device__ bool next_block(int &j) {
     while (cur == 0u && wi > 0) {
       --wi;
-      cur = pair_bits(bm0[wi] | bm1[wi]);
+      cur = bm0[wi] | bm1[wi];
     }
     if (cur == 0u) return false;
     const int bit = 31 - __clz(cur);
     cur &= ~(1u << bit);
-    tile = (wi * 32 + bit) >> 1;
-    const uint32_t w0 = bm0[wi] >> bit, w1 = bm1[wi] >> bit;
-    mask = static_cast<int>((w0 & 1u) | (((w0 >> 1) & 1u) << 1) | ((w1 & 1u) << 2) |
-                            (((w1 >> 1) & 1u) << 3));
+    j = wi * 32 + bit;
+    return true;
+  }
+  // next tile: its two blocks (an odd last block is loaded twice, its second half
+  // unused) and its membership mask; false once the bitmaps run out
+  __device__ bool next(int &ja, int &jb, int &mask) {
+    if (!next_block(ja)) return false;
+    const bool two = next_block(jb);
+    if (!two) jb = ja;
+    auto in = [](const uint32_t *bm, int j) { return static_cast<int>((bm[j >> 5] >> (j & 31)) & 1u); };
+    mask = in(bm0, ja) | ((two ? in(bm0, jb) : 0) << 1) | (in(bm1, ja) << 2) |
+           ((two ? in(bm1, jb) : 0) << 3);
     return true;
   }
 };
@@ -267,7 +273,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   {
     int cnt = 0;
-    for (int w = tid; w < a.n_words; w += kThreads) cnt += __popc(pair_bits(bm0[w] | bm1[w]));
+    for (int w = tid; w < a.n_words; w += kThreads) cnt += __popc(bm0[w] | bm1[w]);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) cnt += __shfl_xor_sync(kFull, cnt, o);
     if (lane == 0 && cnt) atomicAdd(n_blk_tiles_s, cnt);
@@ -275,7 +281,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const int n_blk_t = *n_blk_tiles_s;
+  const int n_blk_t = (*n_blk_tiles_s + 1) / 2;   // listed blocks, two per tile
   const int c0 = min(max(a.col_cnt[bh * a.n_qblk + m0], 0), a.max_col);
   const int c1 = has1 ? min(max(a.col_cnt[bh * a.n_qblk + m1], 0), a.max_col) : 0;
   const int nct0 = (c0 + kKeys - 1) / kKeys, nct1 = (c1 + kKeys - 1) / kKeys;
@@ -305,9 +311,9 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       if (t >= NS && !warp_wait(&empty[st], ((t / NS) - 1) & 1, wc)) break;
       unsigned char *stage = ring + st * L::kTile;
       if (t < n_blk_t) {
-        int tile = 0, mask = 0, ok = 1;
+        int ja = 0, jb = 0, mask = 0, ok = 1;
         if (lane == 0) {
-          ok = walk.next(tile, mask) ? 1 : 0;
+          ok = walk.next(ja, jb, mask) ? 1 : 0;
           if (!ok) *abort_flag = 1;   // count and bitmaps disagree: stop cleanly
         }
         if (!__shfl_sync(kFull, ok, 0)) break;
@@ -315,13 +321,16 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           if (is_k) {
             TileMeta *md = &meta[t % kMetaRing];
             md->kind = 0;
-            md->n = tile;
             md->mask = mask;
-            md->ncols = kKeys;
+            md->blk[0] = ja;
+            md->blk[1] = jb;
           }
+          // rows 0-63 of the tile from block ja, rows 64-127 from block jb, per head-dim half
           mbar_arrive_expect_tx(&full[st], L::kTile);
-          for (int hh = 0; hh < L::kHalves; ++hh)
-            tma_load_4d(stage + hh * L::kHalf, map, &full[st], 64 * hh, g, kKeys * tile, b);
+          for (int hh = 0; hh < L::kHalves; ++hh) {
+            tma_load_4d(stage + hh * L::kHalf, map, &full[st], 64 * hh, g, kBlk * ja, b);
+            tma_load_4d(stage + hh * L::kHalf + L::kHalf / 2, map, &full[st], 64 * hh, g, kBlk * jb, b);
+          }
         }
       } else {
         const int ct = t - n_blk_t;
@@ -345,9 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           for (int i = 0; i < kKeys / 32; ++i) md->pos[lane + 32 * i] = pos[i];
           if (lane == 0) {
             md->kind = 1;
-            md->n = -1;
             md->mask = grp == 0 ? 0x3 : 0xC;
-            md->ncols = ncol;
+            md->blk[0] = md->blk[1] = -1;
           }
         }
         // key row x = lane + 32 i; 16-byte chunk c lies in dims half c >> 3, swizzled in its row
@@ -464,9 +472,10 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       uint32_t valid = 0u;   // bit c: slot c of a 32-slot part is a key of the row
       int lim = 0;
       if (kind == 0) {
-        // a slice lies inside one 64-key half: key kSW * cs + c is in half (kSW * cs) / 64
-        const bool member = (hmask >> ((kSW * cs) >> 6)) & 1;
-        lim = member ? last_key - kKeys * md->n - kSW * cs : -1;   // slots <= lim are keys
+        // slice cs is 64-key half cs, whose slot c holds key 64 * blk[cs] + c
+        static_assert(kSW == kBlk, "one softmax slice per 64-key half");
+        const bool member = (hmask >> cs) & 1;
+        lim = member ? last_key - kBlk * md->blk[cs] : -1;   // slots <= lim are keys
       }
       tmem_wait_ld();
       const bool trim = kind != 0 || lim < kSW - 1;
@@ -677,8 +686,8 @@ cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
   if (!make_map(&a.tq, pa.q, D, pa.H_q, pa.S, pa.B, kRowsQ) ||
-      !make_map(&a.tk, pa.k, D, pa.H_kv, pa.S, pa.B, kKeys) ||
-      !make_map(&a.tv, pa.v, D, pa.H_kv, pa.S, pa.B, kKeys))
+      !make_map(&a.tk, pa.k, D, pa.H_kv, pa.S, pa.B, kBlk) ||
+      !make_map(&a.tv, pa.v, D, pa.H_kv, pa.S, pa.B, kBlk))
     return cudaErrorInvalidValue;
   a.k = static_cast<const uint16_t *>(pa.k);
   a.v = static_cast<const uint16_t *>(pa.v);
