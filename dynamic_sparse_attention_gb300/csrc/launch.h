@@ -147,7 +147,7 @@ struct BsArgs {
   int B, S, H_q, H_kv, D;
   int nb, k_b, max_blk;
   float scale;
-  float *q_pool, *k_pool;                          // scratch [B, H_q|H_kv, nb, D]
+  float *q_pool, *k_pool;   // scratch: q [B, H_q, nb, D], k transposed [B, H_kv, D, nb]
   float *dbg_q_pool, *dbg_k_pool, *dbg_scores;     // optional copies / [B, H_q, nb, nb]
   int32_t *blk_cnt, *blk_idx, *col_cnt;
 };

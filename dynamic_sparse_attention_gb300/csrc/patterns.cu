@@ -17,15 +17,20 @@
 //    piece (8 head dimensions of one head) of the token rows, so every load of a token
 //    row is coalesced across the CTA, and sums it over the block's tokens in fp32.  Q
 //    and K are each read once: this kernel is the HBM-bound part.
-//  * bs_topk_kernel: one CTA per (b, query head, R consecutive query blocks).  The
-//    pooled key blocks stream through shared memory (transposed, 128 at a time); each
-//    thread scores one key block against R/2 of the R pooled query rows with fp32 FMAs
-//    and the rows' scores stay in shared memory.  Then one warp per row finds the
-//    k_b-th largest score by an 8-bit radix select over order-preserving keys and
+//    The pooled keys are stored transposed ([D][nb] per KV head) for the next kernel.
+//  * bs_topk_kernel: one CTA per (b, query head, R consecutive query blocks).  The R
+//    pooled query rows (pre-scaled) sit in shared memory; each thread scores two key
+//    blocks against all R rows with fp32 FMAs, reading the keys' transposed columns
+//    straight from L2 (coalesced across the warp: 4 FMAs per shared-memory load), and
+//    the rows' scores stay in shared memory.  Then one warp per row finds the k_b-th
+//    largest score (value buckets between the row's min and max, exact ranking inside
+//    the boundary bucket, an 8-bit radix select when that bucket is crowded) and
 //    writes the kept blocks in ascending order (larger score first, ties -> smaller
 //    block index).  Softmax is monotone along a row, so the kernel ranks the scaled
 //    logits; the causal mask is the row length m + 1.
 #include <math.h>
+
+#include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
@@ -96,15 +101,20 @@ __global__ void __launch_bounds__(kPoolThreads) bs_pool_kernel(BsArgs a) {
         acc[2 * c + 1] += bf16_hi(w[c]);
       }
     }
-    // pooled layout [B, H, nb, D]
+    // q: [B, H_q, nb, D]; k: transposed [B, H_kv, D, nb]; debug copies [B, H, nb, D]
     const int h = pp / (a.D / 8), d0 = (pp - h * (a.D / 8)) * 8;
     const size_t o = ((static_cast<size_t>(b) * H + h) * a.nb + j) * a.D + d0;
-    float *dst = (is_q ? a.q_pool : a.k_pool) + o;
-    float *dbg = is_q ? a.dbg_q_pool : a.dbg_k_pool;
     const float4 v0 = make_float4(acc[0] * inv, acc[1] * inv, acc[2] * inv, acc[3] * inv);
     const float4 v1 = make_float4(acc[4] * inv, acc[5] * inv, acc[6] * inv, acc[7] * inv);
-    reinterpret_cast<float4 *>(dst)[0] = v0;
-    reinterpret_cast<float4 *>(dst)[1] = v1;
+    if (is_q) {
+      reinterpret_cast<float4 *>(a.q_pool + o)[0] = v0;
+      reinterpret_cast<float4 *>(a.q_pool + o)[1] = v1;
+    } else {
+      float *kt = a.k_pool + (static_cast<size_t>(b) * H + h) * a.D * static_cast<size_t>(a.nb) + j;
+#pragma unroll
+      for (int x = 0; x < 8; ++x) kt[static_cast<size_t>(d0 + x) * a.nb] = acc[x] * inv;
+    }
+    float *dbg = is_q ? a.dbg_q_pool : a.dbg_k_pool;
     if (dbg) {
       reinterpret_cast<float4 *>(dbg + o)[0] = v0;
       reinterpret_cast<float4 *>(dbg + o)[1] = v1;
@@ -115,19 +125,16 @@ __global__ void __launch_bounds__(kPoolThreads) bs_pool_kernel(BsArgs a) {
 // ------------------------------------------------------------------------------ scores + top-k
 
 constexpr int kTopThreads = 256;
-constexpr int kKeyChunk = 128;   // pooled key blocks staged per round
+constexpr int kKeysPerPass = 2 * kTopThreads;   // two key blocks per thread and pass
 
-template <int D>
-struct BsSmem {
-  static constexpr int kTStride = kKeyChunk + 1;   // transposed chunk row (padded)
-  static size_t bytes(int R, int nb) {
-    return (static_cast<size_t>(R) * D + static_cast<size_t>(D) * kTStride +
-            static_cast<size_t>(R) * nb + 8 * 256) * 4;
-  }
-};
+inline size_t bs_smem_bytes(int R, int nb, int D) {
+  return (static_cast<size_t>(R) * D + static_cast<size_t>(R) * nb + 8 * 256) * 4;
+}
 
-// Top-k of s[0 .. n) (n > k) for one warp: writes the kept indices ascending to out.
-__device__ void warp_topk_ascending(const float *s, int n, int k, int *hist, int32_t *out) {
+// Top-k of s[0 .. n) (n > k) for one warp by an 8-bit radix select over the order-
+// preserving keys: writes the kept indices ascending to out.  The general path (any
+// values, many equal ones); warp_topk_bucket below is the usual one.
+__device__ void warp_topk_radix(const float *s, int n, int k, int *hist, int32_t *out) {
   const int lane = threadIdx.x & 31;
   uint32_t prefix = 0u, mask = 0u;
   int need = k;
@@ -193,13 +200,113 @@ __device__ void warp_topk_ascending(const float *s, int n, int k, int *hist, int
   }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kTopThreads) bs_topk_kernel(BsArgs a, int R) {
+// Top-k of s[0 .. n) (n > k) for one warp, ascending into out.  The scores are spread
+// over 256 buckets by value between the row's min and max (a map that never decreases
+// with the score, so a higher bucket holds only larger scores); one histogram and a
+// scan from the top find the bucket holding the k-th largest score; that bucket's
+// members (at most 32, else the radix select runs) are ranked exactly: larger score,
+// then smaller index.  Kept members are marked in s (a NaN pattern no score has), and
+// one pass writes every index above the bucket or marked.
+__device__ void warp_topk_bucket(float *s, int n, int k, int *hist, int32_t *out) {
+  const int lane = threadIdx.x & 31;
+  float mn = INFINITY, mx = -INFINITY;
+  for (int j = lane; j < n; j += 32) {
+    mn = fminf(mn, s[j]);
+    mx = fmaxf(mx, s[j]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mn = fminf(mn, __shfl_xor_sync(kFull, mn, o));
+    mx = fmaxf(mx, __shfl_xor_sync(kFull, mx, o));
+  }
+  const unsigned lt = (1u << lane) - 1u;
+  if (!(mx > mn)) {   // every score equal: the k smallest indices
+    for (int j = lane; j < k; j += 32) out[j] = j;
+    return;
+  }
+  const float sc = 256.f / (mx - mn);
+  auto bucket = [&](float x) { return min(255, static_cast<int>((x - mn) * sc)); };
+  for (int i = lane; i < 256; i += 32) hist[i] = 0;
+  __syncwarp();
+  for (int j = lane; j < n; j += 32) atomicAdd(&hist[bucket(s[j])], 1);
+  __syncwarp();
+  int c[8], sum = 0;
+#pragma unroll
+  for (int u = 0; u < 8; ++u) {
+    c[u] = hist[255 - 8 * lane - u];
+    sum += c[u];
+  }
+  int incl = sum;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int v = __shfl_up_sync(kFull, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const int excl = incl - sum;
+  const int src = __ffs(__ballot_sync(kFull, excl < k && k <= incl)) - 1;
+  int bb = 0, above = 0, members = 0;
+  if (lane == src) {
+    int acc = excl;
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      if (acc + c[u] >= k) {
+        bb = 255 - 8 * lane - u;
+        above = acc;
+        members = c[u];
+        break;
+      }
+      acc += c[u];
+    }
+  }
+  bb = __shfl_sync(kFull, bb, src);
+  above = __shfl_sync(kFull, above, src);
+  members = __shfl_sync(kFull, members, src);
+  const int need = k - above;   // members of bucket bb to keep, 1 .. members
+  if (members > 32) {
+    warp_topk_radix(s, n, k, hist, out);
+    return;
+  }
+  // the bucket's members in index order (hist is free again): lane i takes member i
+  __syncwarp();
+  int got = 0;
+  for (int j0 = 0; j0 < n && got < members; j0 += 32) {
+    const int j = j0 + lane;
+    const bool in = j < n && bucket(s[j]) == bb;
+    const unsigned bal = __ballot_sync(kFull, in);
+    if (in) hist[got + __popc(bal & lt)] = j;
+    got += __popc(bal);
+  }
+  __syncwarp();
+  const int my_j = lane < members ? hist[lane] : -1;
+  const float my_s = my_j >= 0 ? s[my_j] : -INFINITY;
+  int rank = 0;   // members ranked above this one
+  for (int i = 0; i < members; ++i) {
+    const int oj = __shfl_sync(kFull, my_j, i);
+    const float os = __shfl_sync(kFull, my_s, i);
+    rank += (os > my_s || (os == my_s && oj < my_j)) ? 1 : 0;
+  }
+  __syncwarp();
+  if (my_j >= 0 && rank < need) s[my_j] = __uint_as_float(0xffffffffu);
+  __syncwarp();
+  int base = 0;
+  for (int j0 = 0; j0 < n; j0 += 32) {
+    const int j = j0 + lane;
+    bool take = false;
+    if (j < n) {
+      const float x = s[j];
+      take = __float_as_uint(x) == 0xffffffffu || bucket(x) > bb;
+    }
+    const unsigned bt = __ballot_sync(kFull, take);
+    if (take) out[base + __popc(bt & lt)] = j;
+    base += __popc(bt);
+  }
+}
+
+template <int D, int R>
+__global__ void __launch_bounds__(kTopThreads) bs_topk_kernel(BsArgs a) {
   extern __shared__ __align__(16) float fsm[];
-  constexpr int kT = BsSmem<D>::kTStride;
-  float *s_q = fsm;                              // [R][D]
-  float *s_kt = s_q + R * D;                     // [D][kT] pooled keys, transposed
-  float *s_sc = s_kt + D * kT;                   // [R][nb] scores
+  float *s_q = fsm;                              // [R][D], pre-scaled
+  float *s_sc = s_q + R * D;                     // [R][nb] scores
   int *s_hist = reinterpret_cast<int *>(s_sc + static_cast<size_t>(R) * a.nb);   // [8][256]
   const int tid = threadIdx.x, warp = tid >> 5;
   const int bh = blockIdx.y;                     // b * H_q + h
@@ -208,45 +315,37 @@ __global__ void __launch_bounds__(kTopThreads) bs_topk_kernel(BsArgs a, int R) {
   const int m0 = blockIdx.x * R;
   const int rows = min(R, a.nb - m0);
   const float *qp = a.q_pool + (static_cast<size_t>(bh) * a.nb + m0) * D;
-  const float *kp = a.k_pool + (static_cast<size_t>(b) * a.H_kv + g) * a.nb * static_cast<size_t>(D);
+  const float *kt = a.k_pool + (static_cast<size_t>(b) * a.H_kv + g) * D * static_cast<size_t>(a.nb);
   for (int e = tid; e < R * D; e += kTopThreads) s_q[e] = e < rows * D ? qp[e] * a.scale : 0.f;
+  __syncthreads();
   const int n_keys = m0 + rows;                  // the last row's causal limit
-  const int jj = tid & (kKeyChunk - 1), rg = tid >> 7;   // key of the chunk, row group (0/1)
-  const int rpt = (R + 1) / 2;                   // rows per thread: rg, rg + 2, ...
-  for (int kc = 0; kc < n_keys; kc += kKeyChunk) {
-    __syncthreads();   // previous chunk consumed (and s_q written on the first round)
-    const int nk = min(kKeyChunk, n_keys - kc);
-    for (int e = tid; e < nk * (D / 4); e += kTopThreads) {
-      const int r = e / (D / 4), d4 = e - r * (D / 4);
-      const float4 v = reinterpret_cast<const float4 *>(kp + static_cast<size_t>(kc + r) * D)[d4];
-      s_kt[(4 * d4 + 0) * kT + r] = v.x;
-      s_kt[(4 * d4 + 1) * kT + r] = v.y;
-      s_kt[(4 * d4 + 2) * kT + r] = v.z;
-      s_kt[(4 * d4 + 3) * kT + r] = v.w;
-    }
-    __syncthreads();
-    if (jj < nk) {
-      float acc[8];
+  for (int kc = 0; kc < n_keys; kc += kKeysPerPass) {
+    const int j0 = kc + tid, j1 = j0 + kTopThreads;
+    const bool v0 = j0 < n_keys, v1 = j1 < n_keys;
+    if (!v0) break;                              // j1 > j0: nothing left for this thread
+    float acc0[R], acc1[R];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) acc[u] = 0.f;
-      for (int d = 0; d < D; d += 4) {
-        const float k0 = s_kt[(d + 0) * kT + jj], k1 = s_kt[(d + 1) * kT + jj];
-        const float k2 = s_kt[(d + 2) * kT + jj], k3 = s_kt[(d + 3) * kT + jj];
+    for (int r = 0; r < R; ++r) acc0[r] = acc1[r] = 0.f;
+#pragma unroll 4
+    for (int d = 0; d < D; d += 4) {
+      float k0[4], k1[4];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (u < rpt) {
-            const int r = rg + 2 * u;
-            if (r < R) {
-              const float4 qv = *reinterpret_cast<const float4 *>(s_q + r * D + d);
-              acc[u] = fmaf(qv.x, k0, fmaf(qv.y, k1, fmaf(qv.z, k2, fmaf(qv.w, k3, acc[u]))));
-            }
-          }
-        }
+      for (int x = 0; x < 4; ++x) {
+        k0[x] = kt[static_cast<size_t>(d + x) * a.nb + j0];
+        k1[x] = v1 ? kt[static_cast<size_t>(d + x) * a.nb + j1] : 0.f;
       }
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const int r = rg + 2 * u;
-        if (u < rpt && r < rows) s_sc[static_cast<size_t>(r) * a.nb + kc + jj] = acc[u];
+      for (int r = 0; r < R; ++r) {
+        const float4 qv = *reinterpret_cast<const float4 *>(s_q + r * D + d);
+        acc0[r] = fmaf(qv.x, k0[0], fmaf(qv.y, k0[1], fmaf(qv.z, k0[2], fmaf(qv.w, k0[3], acc0[r]))));
+        acc1[r] = fmaf(qv.x, k1[0], fmaf(qv.y, k1[1], fmaf(qv.z, k1[2], fmaf(qv.w, k1[3], acc1[r]))));
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+      if (r < rows) {
+        s_sc[static_cast<size_t>(r) * a.nb + j0] = acc0[r];
+        if (v1) s_sc[static_cast<size_t>(r) * a.nb + j1] = acc1[r];
       }
     }
   }
@@ -255,7 +354,7 @@ __global__ void __launch_bounds__(kTopThreads) bs_topk_kernel(BsArgs a, int R) {
   for (int r = warp; r < rows; r += kTopThreads / 32) {
     const int m = m0 + r;
     const int n = m + 1;
-    const float *sr = s_sc + static_cast<size_t>(r) * a.nb;
+    float *sr = s_sc + static_cast<size_t>(r) * a.nb;
     const size_t row = static_cast<size_t>(bh) * a.nb + m;
     int32_t *out = a.blk_idx + row * a.max_blk;
     const int lane = tid & 31;
@@ -265,7 +364,7 @@ __global__ void __launch_bounds__(kTopThreads) bs_topk_kernel(BsArgs a, int R) {
     if (cnt == n) {
       for (int j = lane; j < n; j += 32) out[j] = j;
     } else if (cnt > 0) {
-      warp_topk_ascending(sr, n, cnt, s_hist + warp * 256, out);
+      warp_topk_bucket(sr, n, cnt, s_hist + warp * 256, out);
     }
     if (lane == 0) {
       a.blk_cnt[row] = cnt;
@@ -284,10 +383,10 @@ cudaError_t launch_ashape(const AshapeArgs &a, cudaStream_t s) {
 }
 
 int bs_rows_per_cta(int nb, int D) {
-  for (int R = 16; R >= 1; R >>= 1) {
-    const size_t smem = D == 128 ? BsSmem<128>::bytes(R, nb) : BsSmem<64>::bytes(R, nb);
-    if (smem <= 200 * 1024) return R;
-  }
+  for (int R = 8; R >= 1; R >>= 1)   // prefer two CTAs per SM, then one
+    if (bs_smem_bytes(R, nb, D) <= 100 * 1024) return R;
+  for (int R = 8; R >= 1; R >>= 1)
+    if (bs_smem_bytes(R, nb, D) <= 200 * 1024) return R;
   return 0;
 }
 
@@ -301,15 +400,24 @@ cudaError_t launch_block_sparse(const BsArgs &a, cudaStream_t s) {
   const int R = bs_rows_per_cta(a.nb, a.D);
   if (R < 1) return cudaErrorInvalidValue;
   const dim3 grid((a.nb + R - 1) / R, a.B * a.H_q);
-  auto go = [&](auto kern, size_t smem) {
+  const size_t smem = bs_smem_bytes(R, a.nb, a.D);
+  auto go = [&](auto kern) {
     cudaError_t st = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (st != cudaSuccess) return st;
     ProfScope ps("bs_score_topk", s);
-    kern<<<grid, kTopThreads, smem, s>>>(a, R);
+    kern<<<grid, kTopThreads, smem, s>>>(a);
     return cudaGetLastError();
   };
-  return a.D == 128 ? go(bs_topk_kernel<128>, BsSmem<128>::bytes(R, a.nb))
-                    : go(bs_topk_kernel<64>, BsSmem<64>::bytes(R, a.nb));
+  auto pick = [&](auto dc) {
+    constexpr int DD = decltype(dc)::value;
+    switch (R) {
+      case 8: return go(bs_topk_kernel<DD, 8>);
+      case 4: return go(bs_topk_kernel<DD, 4>);
+      case 2: return go(bs_topk_kernel<DD, 2>);
+      default: return go(bs_topk_kernel<DD, 1>);
+    }
+  };
+  return a.D == 128 ? pick(std::integral_constant<int, 128>{}) : pick(std::integral_constant<int, 64>{});
 }
 
 }  // namespace dsa

@@ -174,3 +174,20 @@ def test_ashape_128k_config():
         for h in (0, 31):
             assert np.array_equal(_lists(idx, 0, h, m), patterns.ashape_blocks(m, 1024, 4096))
     _check_attention(c, idx, out, lse, [(0, h, m) for h in (0, 17) for m in (0, 80, 2047)])
+
+
+def test_block_sparse_crowded_boundary_bucket():
+    """One key block far above the rest (every query all ones, block 50's keys all 8):
+    in rows m >= 50 the other scores crowd into the lowest value buckets, so the
+    boundary bucket holds more than 32 blocks and the radix select decides."""
+    c = prefill_case("bs_crowd", S=64 * 120, H_q=2, H_kv=1, D=64, seed=74)
+    one = np.uint16(0x3F80)     # 1.0 in bf16
+    eight = np.uint16(0x4100)   # 8.0
+    c.q[:] = one
+    c.k[0, 64 * 50:64 * 51] = eight
+    q, k, v = _dev(c)
+    idx = dsa.block_sparse_index_build(q, k, k_b=10, debug=True)
+    torch.cuda.synchronize()
+    _check_block_sparse(c, idx, 10, range(c.H_q), rows=[0, 9, 10, 49, 50, 51, 80, 119])
+    for m in (50, 80, 119):
+        assert 50 in _lists(idx, 0, 0, m)
