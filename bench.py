@@ -529,7 +529,7 @@ def main():
         for _ in range(2):
             build()
             dsa.sparse_attn_prefill(pq, pk, pv, lists["blk_cnt"], lists["blk_idx"],
-                                    lists["col_cnt"], None, out=pout, lse=plse)
+                                    lists["col_cnt"], lists.get("col_idx"), out=pout, lse=plse)
         ib, at = [], []
         for _ in range(steps):
             flush()
@@ -538,7 +538,7 @@ def main():
             build()
             e1.record()
             dsa.sparse_attn_prefill(pq, pk, pv, lists["blk_cnt"], lists["blk_idx"],
-                                    lists["col_cnt"], None, out=pout, lse=plse)
+                                    lists["col_cnt"], lists.get("col_idx"), out=pout, lse=plse)
             e2.record()
             ib.append((e0, e1))
             at.append((e1, e2))
@@ -546,8 +546,9 @@ def main():
         ib = statistics.mean(a.elapsed_time(b) for a, b in ib)
         at = statistics.mean(a.elapsed_time(b) for a, b in at)
         bc = lists["blk_cnt"].cpu().numpy()
-        fl = accounting.prefill_tile_flops(bc, np.zeros_like(bc), pre.D)
-        return {"index_ms": ib, "attention_ms": at, "tiles": int(bc.sum()),
+        cc = lists["col_cnt"].cpu().numpy()
+        fl = accounting.prefill_tile_flops(bc, cc, pre.D)
+        return {"index_ms": ib, "attention_ms": at, "tiles": int(bc.sum() + np.ceil(cc / 64.0).sum()),
                 "tile_density_vs_causal_dense": float(bc.sum()) / dense_tiles,
                 "tile_flops": fl, "attention_TFLOPs": fl / (at * 1e-3) / 1e12,
                 "attention_tc_frac": fl / (at * 1e-3) / 1e12 / tc_peak}
@@ -568,6 +569,15 @@ def main():
         "block_sparse": dict(time_pattern(lambda: dsa.block_sparse_index_build(
             pq, pk, k_b=100, out=bsl, workspace=ws_bs), pat_steps), k_b=100),
     }
+    mix_pats = [("vertical_slash", "a_shape", "block_sparse")[h % 3] for h in range(pre.H_q)]
+    mix_kw = dict(head_pattern=mix_pats, last_q=pre.last_q, n_vertical=pre.n_vertical,
+                  n_slash=pre.n_slash, n_global=1024, n_local=4096, k_b=100)
+    mix_out = {key: idx[key] for key in ("blk_cnt", "blk_idx", "col_cnt", "col_idx")}
+    ws_mix = torch.empty(max(1, dsa.mixed_index_build_workspace_bytes(pq, pk, **mix_kw)),
+                         dtype=torch.uint8, device=dev)
+    patterns_line["mixed"] = dict(time_pattern(lambda: dsa.mixed_index_build(
+        pq, pk, out=mix_out, workspace=ws_mix, **mix_kw), pat_steps),
+        heads="h mod 3: vertical-slash, A-shape, Block-Sparse")
     pool_bytes = accounting.block_sparse_pool_bytes(1, pre.S, pre.H_q, pre.H_kv, pre.D)
     dsa.profile_enable(True)
     for _ in range(pat_steps):
@@ -672,8 +682,8 @@ def main():
             "chunks_per_stage": stage_chunks,
             "attended_keys": attended,
         },
-        # the same prefill kernel over MInference A-shape (1024 initial + 4096 local tokens)
-        # and Block-Sparse (k_b = 100) lists built on the GPU, same inputs
+        # the same prefill kernel over MInference A-shape (1024 initial + 4096 local tokens),
+        # Block-Sparse (k_b = 100) and a per-head mix of the three patterns, same inputs
         "prefill_patterns": patterns_line,
         # mask caching (InfiniteHiP section 3.4): the same step with stage i recomputed only
         # when step % n_refresh[i] == 0, averaged over whole refresh periods

@@ -19,6 +19,8 @@ from .binding import (  # noqa: F401
     HipSelectCache,
     hip_select_workspace_bytes,
     library_path,
+    mixed_index_build,
+    mixed_index_build_workspace_bytes,
     load,
     profile_collect,
     profile_enable,

@@ -51,6 +51,15 @@ class VsDebug(ctypes.Structure):
     _fields_ = [("vsum", _vp), ("ssum", _vp)]
 
 
+class MixedCfg(ctypes.Structure):
+    _fields_ = [("head_pattern", _vp), ("vs", VsCfg), ("n_global", _c_int), ("n_local", _c_int),
+                ("k_b", _c_int)]
+
+
+PATTERN_VERTICAL_SLASH, PATTERN_A_SHAPE, PATTERN_BLOCK_SPARSE = 0, 1, 2
+_PATTERN_NAMES = {"vertical_slash": 0, "vs": 0, "a_shape": 1, "block_sparse": 2}
+
+
 class BsDebug(ctypes.Structure):
     _fields_ = [("q_pool", _vp), ("k_pool", _vp), ("scores", _vp)]
 
@@ -88,6 +97,9 @@ _SIGNATURES = {
     "block_sparse_index_build_workspace": (_c_int, [_vp, _c_int, ctypes.POINTER(ctypes.c_size_t)]),
     "block_sparse_index_build": (_c_int, [_vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                           _vp, _vp, ctypes.c_size_t, _vp]),
+    "mixed_index_build_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
+    "mixed_index_build": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
+                                   _vp]),
     "sparse_attn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                      _vp, ctypes.c_float, _vp, _vp, _vp]),
     "sparse_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
@@ -516,6 +528,65 @@ def block_sparse_index_build(q, k, *, k_b: int, block: int = 64, max_blk=None,
                                       ctypes.c_size_t(ws.numel()), _stream(stream))
     _check("block_sparse_index_build", st)
     return out
+
+
+def _mixed_cfg(H_q, head_pattern, last_q, n_vertical, n_slash, n_global, n_local, k_b, block):
+    pats = [(_PATTERN_NAMES[p] if isinstance(p, str) else int(p)) for p in head_pattern]
+    if len(pats) != H_q:
+        raise ValueError(f"head_pattern needs {H_q} entries, got {len(pats)}")
+    arr = (ctypes.c_uint8 * H_q)(*pats)
+    cfg = MixedCfg(ctypes.cast(arr, _vp), VsCfg(last_q, n_vertical, n_slash, block), n_global,
+                   n_local, k_b)
+    return cfg, arr, pats
+
+
+def mixed_index_build(q, k, *, head_pattern, last_q: int = 64, n_vertical: int = 1000,
+                      n_slash: int = 6096, n_global: int = 1024, n_local: int = 4096,
+                      k_b: int = 100, block: int = 64, out: dict | None = None, workspace=None,
+                      stream=None):
+    """Per-head patterns (head_pattern: one of "vertical_slash", "a_shape",
+    "block_sparse" or 0/1/2 per query head) into one set of tile/column lists."""
+    lib = load()
+    _need_cuda(q, k)
+    shape = prefill_shape(q, k)
+    B, S, H_q = shape.B, shape.S, shape.H_q
+    cfg, arr, pats = _mixed_cfg(H_q, head_pattern, last_q, n_vertical, n_slash, n_global,
+                                n_local, k_b, block)
+    nq = (S + block - 1) // block
+    dev = q.device
+    if out is None:
+        out = {
+            "blk_cnt": torch.empty(B, H_q, nq, dtype=torch.int32, device=dev),
+            "blk_idx": torch.empty(B, H_q, nq, nq, dtype=torch.int32, device=dev),
+            "col_cnt": torch.empty(B, H_q, nq, dtype=torch.int32, device=dev),
+            "col_idx": torch.empty(B, H_q, nq, max(n_vertical, 1), dtype=torch.int32, device=dev),
+        }
+    n = ctypes.c_size_t()
+    _check("mixed_index_build_workspace",
+           lib.mixed_index_build_workspace(ctypes.byref(shape), ctypes.byref(cfg), ctypes.byref(n)))
+    ws = _workspace(n.value, dev, workspace)
+    st = lib.mixed_index_build(_ptr(q), _ptr(k), ctypes.byref(shape), ctypes.byref(cfg),
+                               _ptr(out["blk_cnt"]), _ptr(out["blk_idx"]), _ptr(out["col_cnt"]),
+                               _ptr(out["col_idx"]), _ptr(ws), ctypes.c_size_t(ws.numel()),
+                               _stream(stream))
+    del arr
+    _check("mixed_index_build", st)
+    return out
+
+
+def mixed_index_build_workspace_bytes(q, k, *, head_pattern, last_q: int = 64,
+                                      n_vertical: int = 1000, n_slash: int = 6096,
+                                      n_global: int = 1024, n_local: int = 4096, k_b: int = 100,
+                                      block: int = 64) -> int:
+    lib = load()
+    shape = prefill_shape(q, k)
+    cfg, arr, _ = _mixed_cfg(shape.H_q, head_pattern, last_q, n_vertical, n_slash, n_global,
+                             n_local, k_b, block)
+    n = ctypes.c_size_t()
+    _check("mixed_index_build_workspace",
+           lib.mixed_index_build_workspace(ctypes.byref(shape), ctypes.byref(cfg), ctypes.byref(n)))
+    del arr
+    return n.value
 
 
 def sparse_attn_prefill(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx, *, scale=None,

@@ -84,6 +84,165 @@ BsWs bs_layout(const dsa_prefill_shape *s, void *base) {
   return w;
 }
 
+cudaError_t run_vs(const void *q, const void *k, const dsa_prefill_shape *shape,
+                   const dsa_vs_cfg *cfg, int32_t *vertical, int32_t *slash, int32_t *blk_cnt,
+                   int32_t *blk_idx, int32_t *col_cnt, int32_t *col_idx, const dsa_vs_debug *dbg,
+                   const VsWs &w, const HeadSet &heads, cudaStream_t stream) {
+  VsArgs a{};
+  a.q = q;
+  a.k = k;
+  a.B = shape->B;
+  a.S = shape->S;
+  a.H_q = shape->H_q;
+  a.H_kv = shape->H_kv;
+  a.D = shape->D;
+  a.last_q = cfg->last_q;
+  a.n_vertical = cfg->n_vertical;
+  a.n_slash = cfg->n_slash;
+  a.scale = 1.0f / std::sqrt(static_cast<float>(shape->D));
+  a.vertical = vertical;
+  a.slash = slash;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  a.col_idx = col_idx;
+  a.row_m = w.row_m;
+  a.row_l = w.row_l;
+  a.part_m = w.part_m;
+  a.part_l = w.part_l;
+  a.vsum = (dbg && dbg->vsum) ? dbg->vsum : w.vsum;
+  a.ssum = (dbg && dbg->ssum) ? dbg->ssum : w.ssum;
+  a.slash_part = w.slash_part;
+  a.n_ktile = w.n_ktile;
+  a.heads = heads;
+  return launch_vs_index(a, stream);
+}
+
+int check_ashape(const dsa_prefill_shape *shape, int n_global, int n_local, int max_blk) {
+  if (n_global < 0 || n_local < 0 || n_global % kBlock || n_local % kBlock)
+    return fail(DSA_ERR_INVALID_ARG, "n_global=%d / n_local=%d must be non-negative multiples of 64",
+                n_global, n_local);
+  const long n_qblk = (shape->S + kBlock - 1) / kBlock;
+  const long need = std::min(n_qblk, static_cast<long>(n_global / kBlock) + n_local / kBlock);
+  if (max_blk < need)
+    return fail(DSA_ERR_INVALID_ARG, "max_blk=%d < %ld blocks per query block", max_blk, need);
+  return DSA_OK;
+}
+
+cudaError_t run_ashape(const dsa_prefill_shape *shape, int n_global, int n_local, int max_blk,
+                       int32_t *blk_cnt, int32_t *blk_idx, int32_t *col_cnt, const HeadSet &heads,
+                       cudaStream_t stream) {
+  AshapeArgs a{};
+  a.BH = shape->B * shape->H_q;
+  a.H_q = shape->H_q;
+  a.n_qblk = (shape->S + kBlock - 1) / kBlock;
+  a.max_blk = max_blk;
+  a.n_global_blk = n_global / kBlock;
+  a.n_local_blk = n_local / kBlock;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  a.heads = heads;
+  return launch_ashape(a, stream);
+}
+
+int check_block_sparse(const dsa_prefill_shape *shape, int k_b, int max_blk) {
+  const int nb = (shape->S + kBlock - 1) / kBlock;
+  if (k_b < 0) return fail(DSA_ERR_INVALID_ARG, "k_b=%d < 0", k_b);
+  if (max_blk < std::min(k_b, nb))
+    return fail(DSA_ERR_INVALID_ARG, "max_blk=%d < min(k_b=%d, n_qblk=%d)", max_blk, k_b, nb);
+  if (bs_rows_per_cta(nb, shape->D) < 1)
+    return fail(DSA_ERR_UNSUPPORTED, "S=%d: a row of %d block scores exceeds shared memory",
+                shape->S, nb);
+  return DSA_OK;
+}
+
+cudaError_t run_block_sparse(const void *q, const void *k, const dsa_prefill_shape *shape, int k_b,
+                             int max_blk, int32_t *blk_cnt, int32_t *blk_idx, int32_t *col_cnt,
+                             const dsa_bs_debug *dbg, const BsWs &w, const HeadSet &heads,
+                             cudaStream_t stream) {
+  BsArgs a{};
+  a.q = q;
+  a.k = k;
+  a.B = shape->B;
+  a.S = shape->S;
+  a.H_q = shape->H_q;
+  a.H_kv = shape->H_kv;
+  a.D = shape->D;
+  a.nb = (shape->S + kBlock - 1) / kBlock;
+  a.k_b = k_b;
+  a.max_blk = max_blk;
+  a.scale = 1.f / std::sqrt(static_cast<float>(shape->D));
+  a.q_pool = w.q_pool;
+  a.k_pool = w.k_pool;
+  a.dbg_q_pool = dbg ? dbg->q_pool : nullptr;
+  a.dbg_k_pool = dbg ? dbg->k_pool : nullptr;
+  a.dbg_scores = dbg ? dbg->scores : nullptr;
+  a.blk_cnt = blk_cnt;
+  a.blk_idx = blk_idx;
+  a.col_cnt = col_cnt;
+  a.heads = heads;
+  return launch_block_sparse(a, stream);
+}
+
+// Mixed per-head patterns: the vertical-slash scratch, its vertical / slash lists and
+// the Block-Sparse pools, each only if some head uses that pattern.
+struct MixedWs {
+  VsWs vs;
+  BsWs bs;
+  int32_t *vertical, *slash;
+  size_t bytes;
+};
+
+bool uses(const dsa_prefill_shape *s, const dsa_mixed_cfg *c, int pattern) {
+  for (int h = 0; h < s->H_q; ++h)
+    if (c->head_pattern[h] == pattern) return true;
+  return false;
+}
+
+HeadSet heads_of(const dsa_prefill_shape *s, const dsa_mixed_cfg *c, int pattern) {
+  HeadSet hs;
+  hs.all = false;
+  for (int h = 0; h < s->H_q; ++h)
+    if (c->head_pattern[h] == pattern) hs.bits[h >> 5] |= 1u << (h & 31);
+  return hs;
+}
+
+MixedWs mixed_layout(const dsa_prefill_shape *s, const dsa_mixed_cfg *c, void *base) {
+  MixedWs w{};
+  char *p = static_cast<char *>(base);
+  size_t off = 0;
+  if (uses(s, c, DSA_PATTERN_VERTICAL_SLASH)) {
+    w.vs = vs_layout(s, p ? p + off : nullptr);
+    off += w.vs.bytes;
+    Carve cv(p ? p + off : nullptr);
+    w.vertical = cv.take<int32_t>(static_cast<size_t>(s->B) * s->H_q * std::max(c->vs.n_vertical, 1));
+    w.slash = cv.take<int32_t>(static_cast<size_t>(s->B) * s->H_q * std::max(c->vs.n_slash, 1));
+    off += cv.bytes();
+  }
+  if (uses(s, c, DSA_PATTERN_BLOCK_SPARSE)) {
+    w.bs = bs_layout(s, p ? p + off : nullptr);
+    off += w.bs.bytes;
+  }
+  w.bytes = off;
+  return w;
+}
+
+int check_mixed(const dsa_prefill_shape *s, const dsa_mixed_cfg *c) {
+  if (!c || !c->head_pattern) return fail(DSA_ERR_INVALID_ARG, "cfg or cfg->head_pattern is NULL");
+  if (s->H_q > 256) return fail(DSA_ERR_UNSUPPORTED, "H_q=%d > 256 heads for a pattern mix", s->H_q);
+  for (int h = 0; h < s->H_q; ++h)
+    if (c->head_pattern[h] > DSA_PATTERN_BLOCK_SPARSE)
+      return fail(DSA_ERR_INVALID_ARG, "head_pattern[%d]=%d is not a pattern", h, c->head_pattern[h]);
+  const int n_qblk = (s->S + kBlock - 1) / kBlock;
+  int st;
+  if (uses(s, c, DSA_PATTERN_VERTICAL_SLASH) && (st = check_vs_cfg(s, &c->vs))) return st;
+  if (uses(s, c, DSA_PATTERN_A_SHAPE) && (st = check_ashape(s, c->n_global, c->n_local, n_qblk)))
+    return st;
+  if (uses(s, c, DSA_PATTERN_BLOCK_SPARSE) && (st = check_block_sparse(s, c->k_b, n_qblk))) return st;
+  return DSA_OK;
+}
+
 }  // namespace
 }  // namespace dsa
 
@@ -122,33 +281,8 @@ int vs_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu",
                 need.bytes, ws_bytes);
   const VsWs w = vs_layout(shape, ws);
-  VsArgs a{};
-  a.q = q;
-  a.k = k;
-  a.B = shape->B;
-  a.S = shape->S;
-  a.H_q = shape->H_q;
-  a.H_kv = shape->H_kv;
-  a.D = shape->D;
-  a.last_q = cfg->last_q;
-  a.n_vertical = cfg->n_vertical;
-  a.n_slash = cfg->n_slash;
-  a.scale = 1.0f / std::sqrt(static_cast<float>(shape->D));
-  a.vertical = vertical;
-  a.slash = slash;
-  a.blk_cnt = blk_cnt;
-  a.blk_idx = blk_idx;
-  a.col_cnt = col_cnt;
-  a.col_idx = col_idx;
-  a.row_m = w.row_m;
-  a.row_l = w.row_l;
-  a.part_m = w.part_m;
-  a.part_l = w.part_l;
-  a.vsum = (dbg && dbg->vsum) ? dbg->vsum : w.vsum;
-  a.ssum = (dbg && dbg->ssum) ? dbg->ssum : w.ssum;
-  a.slash_part = w.slash_part;
-  a.n_ktile = w.n_ktile;
-  cudaError_t e = launch_vs_index(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = run_vs(q, k, shape, cfg, vertical, slash, blk_cnt, blk_idx, col_cnt, col_idx, dbg,
+                         w, HeadSet{}, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "vs_index_build launch");
   return DSA_OK;
 }
@@ -205,25 +339,11 @@ int ashape_index_build(const dsa_prefill_shape *shape, int block, int n_global, 
   int st = check_prefill_shape(shape);
   if (st) return st;
   if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
-  if (n_global < 0 || n_local < 0 || n_global % kBlock || n_local % kBlock)
-    return fail(DSA_ERR_INVALID_ARG, "n_global=%d / n_local=%d must be non-negative multiples of 64",
-                n_global, n_local);
-  const long n_qblk = (shape->S + kBlock - 1) / kBlock;
-  const long need = std::min(n_qblk, static_cast<long>(n_global / kBlock) + n_local / kBlock);
-  if (max_blk < need)
-    return fail(DSA_ERR_INVALID_ARG, "max_blk=%d < %ld blocks per query block", max_blk, need);
+  if ((st = check_ashape(shape, n_global, n_local, max_blk))) return st;
   if (!aligned(blk_cnt, 4) || !aligned(col_cnt, 4) || (max_blk > 0 && !aligned(blk_idx, 4)))
     return fail(DSA_ERR_ALIGNMENT, "list arrays must be non-NULL and 4-byte aligned");
-  AshapeArgs a{};
-  a.BH = shape->B * shape->H_q;
-  a.n_qblk = static_cast<int>(n_qblk);
-  a.max_blk = max_blk;
-  a.n_global_blk = n_global / kBlock;
-  a.n_local_blk = n_local / kBlock;
-  a.blk_cnt = blk_cnt;
-  a.blk_idx = blk_idx;
-  a.col_cnt = col_cnt;
-  cudaError_t e = launch_ashape(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = run_ashape(shape, n_global, n_local, max_blk, blk_cnt, blk_idx, col_cnt, HeadSet{},
+                             static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "ashape_index_build launch");
   return DSA_OK;
 }
@@ -246,13 +366,7 @@ int block_sparse_index_build(const void *q, const void *k, const dsa_prefill_sha
   int st = check_prefill_shape(shape);
   if (st) return st;
   if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
-  const int nb = (shape->S + kBlock - 1) / kBlock;
-  if (k_b < 0) return fail(DSA_ERR_INVALID_ARG, "k_b=%d < 0", k_b);
-  if (max_blk < std::min(k_b, nb))
-    return fail(DSA_ERR_INVALID_ARG, "max_blk=%d < min(k_b=%d, n_qblk=%d)", max_blk, k_b, nb);
-  if (bs_rows_per_cta(nb, shape->D) < 1)
-    return fail(DSA_ERR_UNSUPPORTED, "S=%d: a row of %d block scores exceeds shared memory",
-                shape->S, nb);
+  if ((st = check_block_sparse(shape, k_b, max_blk))) return st;
   if (!aligned(q, 16) || !aligned(k, 16))
     return fail(DSA_ERR_ALIGNMENT, "q and k must be non-NULL and 16-byte aligned");
   if (!aligned(blk_cnt, 4) || !aligned(col_cnt, 4) || (max_blk > 0 && !aligned(blk_idx, 4)))
@@ -265,28 +379,55 @@ int block_sparse_index_build(const void *q, const void *k, const dsa_prefill_sha
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu", need,
                 ws_bytes);
   const BsWs w = bs_layout(shape, ws);
-  BsArgs a{};
-  a.q = q;
-  a.k = k;
-  a.B = shape->B;
-  a.S = shape->S;
-  a.H_q = shape->H_q;
-  a.H_kv = shape->H_kv;
-  a.D = shape->D;
-  a.nb = nb;
-  a.k_b = k_b;
-  a.max_blk = max_blk;
-  a.scale = 1.f / std::sqrt(static_cast<float>(shape->D));
-  a.q_pool = w.q_pool;
-  a.k_pool = w.k_pool;
-  a.dbg_q_pool = dbg ? dbg->q_pool : nullptr;
-  a.dbg_k_pool = dbg ? dbg->k_pool : nullptr;
-  a.dbg_scores = dbg ? dbg->scores : nullptr;
-  a.blk_cnt = blk_cnt;
-  a.blk_idx = blk_idx;
-  a.col_cnt = col_cnt;
-  cudaError_t e = launch_block_sparse(a, static_cast<cudaStream_t>(stream));
+  cudaError_t e = run_block_sparse(q, k, shape, k_b, max_blk, blk_cnt, blk_idx, col_cnt, dbg, w,
+                                   HeadSet{}, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "block_sparse_index_build launch");
+  return DSA_OK;
+}
+
+int mixed_index_build_workspace(const dsa_prefill_shape *shape, const dsa_mixed_cfg *cfg,
+                                size_t *bytes) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if ((st = check_mixed(shape, cfg))) return st;
+  if (!bytes) return fail(DSA_ERR_ALIGNMENT, "bytes is NULL");
+  *bytes = mixed_layout(shape, cfg, nullptr).bytes;
+  return DSA_OK;
+}
+
+int mixed_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
+                      const dsa_mixed_cfg *cfg, int32_t *blk_cnt, int32_t *blk_idx,
+                      int32_t *col_cnt, int32_t *col_idx, void *ws, size_t ws_bytes,
+                      void *stream) {
+  clear_error();
+  int st = check_prefill_shape(shape);
+  if (st) return st;
+  if ((st = check_mixed(shape, cfg))) return st;
+  const bool any_vs = uses(shape, cfg, DSA_PATTERN_VERTICAL_SLASH);
+  if (!aligned(q, 16) || !aligned(k, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q and k must be non-NULL and 16-byte aligned");
+  if (!aligned(blk_cnt, 4) || !aligned(blk_idx, 4) || !aligned(col_cnt, 4) ||
+      (any_vs && cfg->vs.n_vertical > 0 && !aligned(col_idx, 4)))
+    return fail(DSA_ERR_ALIGNMENT, "list arrays must be non-NULL and 4-byte aligned");
+  const size_t need = mixed_layout(shape, cfg, nullptr).bytes;
+  if (ws_bytes < need || (need > 0 && !aligned(ws, 16)))
+    return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu", need,
+                ws_bytes);
+  const MixedWs w = mixed_layout(shape, cfg, ws);
+  const int n_qblk = (shape->S + kBlock - 1) / kBlock;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaSuccess;
+  if (uses(shape, cfg, DSA_PATTERN_A_SHAPE))
+    e = run_ashape(shape, cfg->n_global, cfg->n_local, n_qblk, blk_cnt, blk_idx, col_cnt,
+                   heads_of(shape, cfg, DSA_PATTERN_A_SHAPE), s);
+  if (e == cudaSuccess && uses(shape, cfg, DSA_PATTERN_BLOCK_SPARSE))
+    e = run_block_sparse(q, k, shape, cfg->k_b, n_qblk, blk_cnt, blk_idx, col_cnt, nullptr, w.bs,
+                         heads_of(shape, cfg, DSA_PATTERN_BLOCK_SPARSE), s);
+  if (e == cudaSuccess && any_vs)
+    e = run_vs(q, k, shape, &cfg->vs, w.vertical, w.slash, blk_cnt, blk_idx, col_cnt, col_idx,
+               nullptr, w.vs, heads_of(shape, cfg, DSA_PATTERN_VERTICAL_SLASH), s);
+  if (e != cudaSuccess) return cuda_fail(e, "mixed_index_build launch");
   return DSA_OK;
 }
 

@@ -97,6 +97,16 @@ cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t s);
 // workspace floats of the split path (0 on the cluster path)
 size_t decode_ws_floats(const DecodePlan &p, int B, int T_q, int H_q, int D);
 
+// The query heads an index builder writes (per-head pattern mixes); every head when
+// `all`, else heads < 256 whose bit is set.
+struct HeadSet {
+  bool all = true;
+  uint32_t bits[8] = {};
+  __host__ __device__ bool has(int h) const {
+    return all || (h < 256 && ((bits[h >> 5] >> (h & 31)) & 1u));
+  }
+};
+
 // Vertical-slash index build.
 struct VsArgs {
   const void *q, *k;
@@ -111,6 +121,7 @@ struct VsArgs {
   float *vsum, *ssum;         // [B, H_q, S] column sums / diagonal sums
   float *slash_part;          // [B, H_q, n_ktile, 127] per key-tile diagonal sums
   int n_ktile;
+  HeadSet heads;              // heads whose lists are written (the estimate covers all)
 };
 cudaError_t launch_vs_index(const VsArgs &a, cudaStream_t s);
 constexpr int kVsKeyTile = 64;
@@ -135,7 +146,8 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 // MInference A-shape block lists (static: the initial blocks plus a band ending at the
 // diagonal block).
 struct AshapeArgs {
-  int BH, n_qblk, max_blk;
+  int BH, H_q, n_qblk, max_blk;
+  HeadSet heads;
   int n_global_blk, n_local_blk;
   int32_t *blk_cnt, *blk_idx, *col_cnt;
 };
@@ -150,6 +162,7 @@ struct BsArgs {
   float *q_pool, *k_pool;   // scratch: q [B, H_q, nb, D], k transposed [B, H_kv, D, nb]
   float *dbg_q_pool, *dbg_k_pool, *dbg_scores;     // optional copies / [B, H_q, nb, nb]
   int32_t *blk_cnt, *blk_idx, *col_cnt;
+  HeadSet heads;                                   // query heads pooled, scored and written
 };
 cudaError_t launch_block_sparse(const BsArgs &a, cudaStream_t s);
 // query blocks per CTA of the scoring kernel (0: nb too large for shared memory)

@@ -47,6 +47,7 @@ __global__ void __launch_bounds__(256) ashape_kernel(AshapeArgs a) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int m = blockIdx.x * 8 + warp;
   if (m >= a.n_qblk) return;
+  if (!a.heads.has(static_cast<int>(blockIdx.y) % a.H_q)) return;
   const size_t row = static_cast<size_t>(blockIdx.y) * a.n_qblk + m;
   const int n_init = min(a.n_global_blk, m + 1);             // blocks 0 .. n_init - 1
   const int band_lo = max(n_init, m - a.n_local_blk + 1);     // band blocks band_lo .. m
@@ -73,6 +74,7 @@ __global__ void __launch_bounds__(kPoolThreads) bs_pool_kernel(BsArgs a) {
     const bool is_q = p < pq;
     const int pp = is_q ? p : p - pq;
     const int H = is_q ? a.H_q : a.H_kv;
+    if (is_q && !a.heads.has(pp / (a.D / 8))) continue;   // a head of another pattern
     const uint16_t *src = static_cast<const uint16_t *>(is_q ? a.q : a.k) +
                           (static_cast<size_t>(b) * a.S + t0) * H * a.D + static_cast<size_t>(pp) * 8;
     const size_t stride = static_cast<size_t>(H) * a.D;
@@ -311,6 +313,7 @@ __global__ void __launch_bounds__(kTopThreads) bs_topk_kernel(BsArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5;
   const int bh = blockIdx.y;                     // b * H_q + h
   const int b = bh / a.H_q, h = bh - b * a.H_q;
+  if (!a.heads.has(h)) return;                   // a head of another pattern
   const int g = h / (a.H_q / a.H_kv);
   const int m0 = blockIdx.x * R;
   const int rows = min(R, a.nb - m0);

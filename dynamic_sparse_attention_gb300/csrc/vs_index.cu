@@ -309,7 +309,7 @@ __global__ void vs_slash_kernel(VsArgs a, int r_q) {
   const int o = blockIdx.x * blockDim.x + threadIdx.x;
   const int h = blockIdx.y, b = blockIdx.z;
   const int S = a.S;
-  if (o >= S) return;
+  if (o >= S || !a.heads.has(h)) return;
   // tile t covers offsets [S - r_q - 64t - 63, S - r_q - 64t + 63]
   const int base = S - r_q - (kKT - 1) - o;        // = 64t - u  for a covering tile
   int t_lo = base > 0 ? (base + kKT - 1) / kKT : 0;
@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kTopkNT) vs_topk_kernel(VsArgs a) {
   __shared__ uint32_t s_res[2];
   __shared__ int s_warp[NT / 32 + 1];
   const int bh = blockIdx.x;                   // b * H_q + h
+  if (!a.heads.has(bh % a.H_q)) return;        // a head of another pattern
   const bool is_slash = blockIdx.y == 1;
   const int S = a.S;
   const float *x = (is_slash ? a.ssum : a.vsum) + static_cast<size_t>(bh) * S;
@@ -371,6 +372,7 @@ __global__ void __launch_bounds__(kConvNT) vs_convert_kernel(VsArgs a, int n_qbl
   int *s_d = s_wpre + n_words;
   int *s_vert = s_d + n_qblk;
   const int h = blockIdx.y, b = blockIdx.z;
+  if (!a.heads.has(h)) return;   // a head of another pattern
   const size_t bh = static_cast<size_t>(b) * a.H_q + h;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   for (int w = tid; w < n_words; w += kConvNT) s_bits[w] = 0u;

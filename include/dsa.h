@@ -10,6 +10,7 @@
  *            ashape_index_build  -- MInference A-shape lists (initial blocks + band)
  *            block_sparse_index_build -- MInference Block-Sparse estimate (mean-pooled
  *                                   blocks, top-k_b key blocks per query block)
+ *            mixed_index_build   -- one of the three patterns per head
  *            sparse_attn_prefill -- causal attention over those 64x64 tiles and
  *                                   gathered columns
  *
@@ -278,6 +279,41 @@ int block_sparse_index_build(const void *q, const void *k, const dsa_prefill_sha
                              int block, int k_b, int max_blk, int32_t *blk_cnt, int32_t *blk_idx,
                              int32_t *col_cnt, const dsa_bs_debug *dbg, void *ws, size_t ws_bytes,
                              void *stream);
+
+/* Mixed per-head patterns: MInference assigns each attention head one of its three
+ * patterns (MInference summary, "The Three Sparse Patterns"; the assignment itself
+ * comes from an offline search that needs a model and is an input here). */
+enum {
+  DSA_PATTERN_VERTICAL_SLASH = 0,
+  DSA_PATTERN_A_SHAPE = 1,
+  DSA_PATTERN_BLOCK_SPARSE = 2
+};
+
+typedef struct {
+  const uint8_t *head_pattern;  /* HOST array [H_q] of DSA_PATTERN_* (read during the call) */
+  dsa_vs_cfg vs;                /* vertical-slash heads (block must be 64) */
+  int n_global, n_local;        /* A-shape heads: token counts, multiples of 64 */
+  int k_b;                      /* Block-Sparse heads */
+} dsa_mixed_cfg;
+
+int mixed_index_build_workspace(const dsa_prefill_shape *shape, const dsa_mixed_cfg *cfg,
+                                size_t *bytes);
+
+/* mixed_index_build -- every head's lists by its own pattern, into one set of arrays:
+ * each head's rows are exactly what vs_index_build, ashape_index_build or
+ * block_sparse_index_build writes for that head (the vertical-slash estimate still
+ * runs over every head of a KV group that holds a vertical-slash head).
+ *   blk_cnt [B, H_q, n_qblk], blk_idx [B, H_q, n_qblk, n_qblk] ascending key blocks,
+ *   col_cnt [B, H_q, n_qblk] (0 for A-shape and Block-Sparse heads),
+ *   col_idx [B, H_q, n_qblk, vs.n_vertical] (NULL allowed when no head is
+ *   vertical-slash or vs.n_vertical = 0); pass max_blk = n_qblk and
+ *   max_col = vs.n_vertical to sparse_attn_prefill.
+ * H_q above 256 is UNSUPPORTED; a pattern value outside DSA_PATTERN_* and the checks
+ * of each used pattern's own builder are INVALID_ARG / UNSUPPORTED as there. */
+int mixed_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
+                      const dsa_mixed_cfg *cfg, int32_t *blk_cnt, int32_t *blk_idx,
+                      int32_t *col_cnt, int32_t *col_idx, void *ws, size_t ws_bytes,
+                      void *stream);
 
 /* sparse_attn_prefill -- causal attention of each query block over its listed
  * 64x64 key tiles, then its listed columns gathered 64 at a time, with one

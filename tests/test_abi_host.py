@@ -172,3 +172,30 @@ def test_pattern_builders_validate_arguments(lib):
     big = _pshape(S=4 << 20)
     assert lib.block_sparse_index_build(ok, ok, ctypes.byref(big), 64, 10, 10, ok, ok, ok, None, ok,
                                         ctypes.c_size_t(1 << 40), None) == -2
+
+
+def test_mixed_patterns_validate_arguments(lib):
+    s = _pshape(H_q=4, H_kv=2)
+    n = ctypes.c_size_t()
+
+    def cfg(pats, **kw):
+        arr = (ctypes.c_uint8 * len(pats))(*pats)
+        c = binding.MixedCfg(ctypes.cast(arr, ctypes.c_void_p), binding.VsCfg(64, 100, 200, 64),
+                             kw.get("n_global", 1024), kw.get("n_local", 4096), kw.get("k_b", 100))
+        return c, arr
+
+    c, keep = cfg([1, 1, 1, 1])
+    assert lib.mixed_index_build_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == 0
+    assert n.value == 0                      # A-shape heads need no scratch
+    c, keep = cfg([2, 1, 1, 1])
+    assert lib.mixed_index_build_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == 0
+    assert n.value >= 4 * 64 * 128 * 6       # pooled q and k
+    c, keep = cfg([0, 1, 2, 3])
+    assert lib.mixed_index_build_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == -1
+    c, keep = cfg([1, 1, 0, 0], n_global=100)
+    assert lib.mixed_index_build_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == -1
+    c, keep = cfg([0, 0, 0, 0], n_global=100)  # A-shape settings unused: fine
+    assert lib.mixed_index_build_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == 0
+    big = _pshape(H_q=512, H_kv=8)
+    c, keep = cfg([1] * 512)
+    assert lib.mixed_index_build_workspace(ctypes.byref(big), ctypes.byref(c), ctypes.byref(n)) == -2

@@ -191,3 +191,44 @@ def test_block_sparse_crowded_boundary_bucket():
     _check_block_sparse(c, idx, 10, range(c.H_q), rows=[0, 9, 10, 49, 50, 51, 80, 119])
     for m in (50, 80, 119):
         assert 50 in _lists(idx, 0, 0, m)
+
+
+# ------------------------------------------------------------ mixed per-head patterns
+
+@pytest.mark.parametrize("S,D,G", [(1000, 128, 4), (700, 64, 1)])
+def test_mixed_heads_equal_their_single_pattern_builders(S, D, G):
+    H_kv = 2
+    H_q = H_kv * G
+    c = prefill_case("mixed", B=2, S=S, H_q=H_q, H_kv=H_kv, D=D, seed=75 + S,
+                     n_vertical=40, n_slash=150)
+    q, k, v = _dev(c)
+    pats = [("vertical_slash", "a_shape", "block_sparse")[h % 3] for h in range(H_q)]
+    mix = dsa.mixed_index_build(q, k, head_pattern=pats, n_vertical=40, n_slash=150,
+                                n_global=128, n_local=256, k_b=5)
+    vs_idx = dsa.vs_index_build(q, k, n_vertical=40, n_slash=150)
+    ash = dsa.ashape_index_build(q, k, n_global=128, n_local=256)
+    bsp = dsa.block_sparse_index_build(q, k, k_b=5)
+    out, lse = dsa.sparse_attn_prefill(q, k, v, mix["blk_cnt"], mix["blk_idx"], mix["col_cnt"],
+                                       mix["col_idx"])
+    torch.cuda.synchronize()
+    nq = (S + 63) // 64
+    for b in range(2):
+        for h in range(H_q):
+            ref = {"vertical_slash": vs_idx, "a_shape": ash, "block_sparse": bsp}[pats[h]]
+            for m in range(nq):
+                nb_, nc = int(mix["blk_cnt"][b, h, m]), int(mix["col_cnt"][b, h, m])
+                assert nb_ == int(ref["blk_cnt"][b, h, m])
+                assert torch.equal(mix["blk_idx"][b, h, m, :nb_], ref["blk_idx"][b, h, m, :nb_])
+                if pats[h] == "vertical_slash":
+                    assert nc == int(ref["col_cnt"][b, h, m])
+                    assert torch.equal(mix["col_idx"][b, h, m, :nc], ref["col_idx"][b, h, m, :nc])
+                else:
+                    assert nc == 0
+    o = out.float().cpu().numpy()
+    for (b, h, m) in [(0, h, m) for h in range(H_q) for m in (0, nq // 2, nq - 1)]:
+        nb_, nc = int(mix["blk_cnt"][b, h, m]), int(mix["col_cnt"][b, h, m])
+        O64, _ = vs.prefill_block_attention(c.q[b], c.k[b], c.v[b], h, c.G, m,
+                                            mix["blk_idx"][b, h, m, :nb_].cpu().numpy(),
+                                            mix["col_idx"][b, h, m, :nc].cpu().numpy(), c.S, c.scale)
+        mx, mn = attention_errors(o[b, 64 * m:64 * m + len(O64), h], O64)
+        assert mx <= MAX_ABS and mn <= MEAN_ABS
