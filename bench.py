@@ -43,7 +43,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 CACHE_PRESETS = {"default": (16, 8, 4, 4), "flash": (96, 24, 8, 8)}
 NCU_TRAFFIC = {
     ("hip_stage_score_s0", "decode_gqa_T1048576"): 200670720 + 5314560,
-    ("prefill_attention_tc", "prefill_vs_S131072"): 4342883328 + 1074967552,
+    ("prefill_attention_tc", "prefill_vs_S131072"): 4348859392 + 1075625472,
 }
 
 
