@@ -447,6 +447,45 @@ def main():
                                        or "none": statistics.mean(v_) for m, v_ in us.items()},
         }
 
+    # ---------------- FP8 E4M3 keys and values: the same step over the cache rounded to
+    # E4M3 on the device (torch's float8 conversion: nearest, ties to even)
+    k8 = k.to(torch.float8_e4m3fn).view(torch.uint8)
+    v8 = v.to(torch.float8_e4m3fn).view(torch.uint8)
+    s8_idx, s8_cnt = torch.empty_like(sel_idx), torch.empty_like(sel_cnt)
+    ws_sel8 = torch.empty(dsa.hip_select_workspace_bytes(q, k8, cfg), dtype=torch.uint8, device=dev)
+
+    def decode_step_fp8():
+        dsa.hip_select(q, k8, kv_len, cfg, out=(s8_idx, s8_cnt), workspace=ws_sel8)
+        dsa.sparse_attn_decode(q, k8, v8, kv_len, s8_idx, s8_cnt, n_sink=dec.n_sink,
+                               n_stream=dec.n_stream, out=out, lse=lse, workspace=ws_dec)
+
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        for _ in range(3):
+            decode_step_fp8()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    graph8 = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph8):
+        decode_step_fp8()
+    fp8_ms = []
+    for _ in range(max(3, args.steps)):
+        flush()
+        e0, e1 = ev(), ev()
+        e0.record()
+        graph8.replay()
+        e1.record()
+        fp8_ms.append((e0, e1))
+    torch.cuda.synchronize()
+    fp8_us = 1e3 * statistics.mean(a.elapsed_time(b_) for a, b_ in fp8_ms)
+    dsa.profile_enable(True)
+    for _ in range(max(3, args.steps)):
+        flush()
+        decode_step_fp8()
+    torch.cuda.synchronize()
+    dsa.profile_enable(False)
+    k8stats = dsa.profile_collect()
+
     # ---------------- per-kernel durations (CUDA events on the launch stream)
     dsa.profile_enable(True)
     for _ in range(args.steps):
@@ -462,26 +501,34 @@ def main():
     kern = {name: {"launches": n, "avg_us": 1e3 * t / n} for name, (n, t) in kstats.items()}
 
     # ---------------- algorithmic work (from one debug run of the same inputs)
-    sel2, cnt2, dbg = dsa.hip_select(q, k, kv_len, cfg, debug=True)
-    torch.cuda.synchronize()
-    T = int(dec.kv_len[0])
+    def decode_work(kk, elem):
+        """Per-stage bytes (tournament rows + index list + scores + query), the tournament
+        rows, the chunk counts, the attention bytes and the attended key count of one
+        step over key rows of `elem` bytes per element (bf16 queries)."""
+        sel2, cnt2, dbg = dsa.hip_select(q, kk, kv_len, cfg, debug=True)
+        torch.cuda.synchronize()
+        T = int(dec.kv_len[0])
+        prev = np.arange(dec.n_sink, max(dec.n_sink, T - dec.n_stream))
+        s_bytes, s_rows, s_chunks = [], [], []
+        for i, L in enumerate(dec.chunk):
+            n = -(-len(prev) // L)
+            chunks = [prev[j * L:(j + 1) * L] for j in range(n)]
+            lens = np.array([len(c) for c in chunks], np.int64)
+            reps = dbg["rep"][i][0, :, :n].cpu().numpy().astype(np.int64)
+            rows = accounting.stage_rows(reps, None, chunks, lens, dec.G)
+            s_rows.append(rows)
+            s_chunks.append(n)
+            idx_bytes = 0 if i == 0 else 4 * len(prev)
+            s_bytes.append(rows * dec.D * elem + idx_bytes + 4 * n + dec.T_q * dec.H_q * dec.D * 2)
+            cnt = int(dbg["stage_cnt"][i][0])
+            prev = dbg["stage_idx"][i][0, :cnt].cpu().numpy()
+        n_att = min(dec.n_sink, T) + int(cnt2[0]) + (T - max(dec.n_sink, T - dec.n_stream))
+        a_bytes = n_att * dec.H_kv * dec.D * elem * 2 + 2 * dec.T_q * dec.H_q * dec.D * 2
+        return s_bytes, s_rows, s_chunks, a_bytes, n_att
+
     elem = 2
-    prev = np.arange(dec.n_sink, max(dec.n_sink, T - dec.n_stream))
-    stage_bytes, stage_rows, stage_chunks = [], [], []
-    for i, L in enumerate(dec.chunk):
-        n = -(-len(prev) // L)
-        chunks = [prev[j * L:(j + 1) * L] for j in range(n)]
-        lens = np.array([len(c) for c in chunks], np.int64)
-        reps = dbg["rep"][i][0, :, :n].cpu().numpy().astype(np.int64)
-        rows = accounting.stage_rows(reps, None, chunks, lens, dec.G)
-        stage_rows.append(rows)
-        stage_chunks.append(n)
-        idx_bytes = 0 if i == 0 else 4 * len(prev)
-        stage_bytes.append(rows * dec.D * elem + idx_bytes + 4 * n + dec.T_q * dec.H_q * dec.D * elem)
-        cnt = int(dbg["stage_cnt"][i][0])
-        prev = dbg["stage_idx"][i][0, :cnt].cpu().numpy()
-    attended = min(dec.n_sink, T) + int(cnt2[0]) + (T - max(dec.n_sink, T - dec.n_stream))
-    attn_bytes = attended * dec.H_kv * dec.D * elem * 2 + 2 * dec.T_q * dec.H_q * dec.D * elem
+    T = int(dec.kv_len[0])
+    stage_bytes, stage_rows, stage_chunks, attn_bytes, attended = decode_work(k, elem)
     step_bytes = sum(r * dec.D * elem for r in stage_rows) + attn_bytes
     dec_kernel_bytes = {f"hip_stage_score_s{i}": b for i, b in enumerate(stage_bytes)}
     for name in ("decode_splitk", "decode_cluster_mma"):   # whichever attention kernel ran
@@ -492,6 +539,22 @@ def main():
             kern[name]["achieved_GBps"] = b / (kern[name]["avg_us"] * 1e-6) / 1e9
 
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    sb8, sr8, _, ab8, att8 = decode_work(k8, 1)
+    k8b = {f"hip_stage_score_s{i}": b_ for i, b_ in enumerate(sb8)}
+    k8b["decode_cluster_mma_fp8"] = ab8
+    fp8_kern = {}
+    for name, (n_, t_) in k8stats.items():
+        e_ = {"launches": n_, "avg_us": 1e3 * t_ / n_}
+        if name in k8b:
+            e_["algorithmic_bytes"] = k8b[name]
+            e_["achieved_GBps"] = k8b[name] / (e_["avg_us"] * 1e-6) / 1e9
+            e_["hbm_frac"] = e_["achieved_GBps"] / hbm
+        fp8_kern[name] = e_
+    step8 = sum(r * dec.D for r in sr8) + ab8
+    fp8_line = {"us_per_step_graph": fp8_us, "algorithmic_bytes_per_step": step8,
+                "step_hbm_frac": step8 / (fp8_us * 1e-6) / 1e9 / hbm, "attended_keys": att8,
+                "tournament_rows_per_stage": sr8, "kernels": fp8_kern,
+                "kv": "E4M3 codes rounded on the device from the bf16 cache (torch float8_e4m3fn)"}
     dec_names = [n for n in kern if n.startswith("hip_") or n.startswith("decode_")]
     dom = max(dec_names, key=lambda n: kern[n]["avg_us"] * kern[n]["launches"])
     dom_bytes = dec_kernel_bytes.get(dom)
@@ -685,6 +748,8 @@ def main():
         # the same prefill kernel over MInference A-shape (1024 initial + 4096 local tokens),
         # Block-Sparse (k_b = 100) and a per-head mix of the three patterns, same inputs
         "prefill_patterns": patterns_line,
+        # the same decode step over an FP8 E4M3 copy of the KV cache (bf16 queries)
+        "decode_fp8kv": fp8_line,
         # mask caching (InfiniteHiP section 3.4): the same step with stage i recomputed only
         # when step % n_refresh[i] == 0, averaged over whole refresh periods
         "decode_cached": cached,

@@ -17,7 +17,7 @@ import torch
 from . import _build
 
 MAX_STAGES = 8
-BF16, F32 = 0, 1
+BF16, F32, BF16_FP8KV = 0, 1, 2   # dsa_dtype
 
 _c_int = ctypes.c_int
 _vp = ctypes.c_void_p
@@ -221,9 +221,21 @@ class HipConfig:
         return cfg
 
 
+def _is_fp8(t: torch.Tensor) -> bool:
+    return t.dtype == torch.uint8 or t.dtype == getattr(torch, "float8_e4m3fn", None)
+
+
 def decode_shape(q: torch.Tensor, k: torch.Tensor) -> DecodeShape:
+    """q bf16 / fp32 with k of the same type, or q bf16 with k FP8 E4M3 (a uint8 or
+    float8_e4m3fn tensor of codes)."""
     B, T_q, H_q, D = q.shape
     T_max, H_kv = k.shape[1], k.shape[2]
+    if _is_fp8(k):
+        if q.dtype != torch.bfloat16:
+            raise TypeError("FP8 keys and values need a bfloat16 query")
+        return DecodeShape(B, T_max, T_q, H_q, H_kv, D, BF16_FP8KV)
+    if k.dtype != q.dtype:
+        raise TypeError(f"k ({k.dtype}) must have the type of q ({q.dtype})")
     return DecodeShape(B, T_max, T_q, H_q, H_kv, D, _dtype_code(q))
 
 

@@ -25,8 +25,10 @@ int check_decode_shape(const dsa_decode_shape *s) {
     return fail(DSA_ERR_INVALID_ARG, "H_q=%d must be a positive multiple of H_kv=%d", s->H_q, s->H_kv);
   if (s->H_q > 128) return fail(DSA_ERR_UNSUPPORTED, "H_q=%d > 128", s->H_q);
   if (s->D != 64 && s->D != 128) return fail(DSA_ERR_UNSUPPORTED, "D=%d not in {64, 128}", s->D);
-  if (s->dtype != DSA_BF16 && s->dtype != DSA_F32)
-    return fail(DSA_ERR_UNSUPPORTED, "dtype=%d not DSA_BF16/DSA_F32", s->dtype);
+  if (s->dtype != DSA_BF16 && s->dtype != DSA_F32 && s->dtype != DSA_BF16_FP8KV)
+    return fail(DSA_ERR_UNSUPPORTED, "dtype=%d not DSA_BF16 / DSA_F32 / DSA_BF16_FP8KV", s->dtype);
+  if (s->dtype == DSA_BF16_FP8KV && s->D != 128)
+    return fail(DSA_ERR_UNSUPPORTED, "FP8 keys and values: D=%d, only 128", s->D);
   return DSA_OK;
 }
 
@@ -225,6 +227,8 @@ int sparse_attn_decode_workspace(const dsa_decode_shape *shape, int max_sel, int
   const long a_max = attended_max(shape, max_sel, n_sink, n_stream);
   if (a_max > 0x7fffffffL) return fail(DSA_ERR_INVALID_ARG, "attended set too large");
   const int R = (shape->H_q / shape->H_kv) * shape->T_q;
+  if (shape->dtype == DSA_BF16_FP8KV && R > 16)
+    return fail(DSA_ERR_UNSUPPORTED, "FP8 keys and values: (H_q/H_kv)*T_q = %d > 16", R);
   const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
   const size_t nf = decode_ws_floats(plan, shape->B, shape->T_q, shape->H_q, shape->D);
   Carve cv(nullptr);
@@ -246,6 +250,8 @@ int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_
   const int R = (shape->H_q / shape->H_kv) * shape->T_q;
   if (R * shape->D > 4096)
     return fail(DSA_ERR_UNSUPPORTED, "(H_q/H_kv)*T_q*D = %d > 4096 rows*dims per KV head", R * shape->D);
+  if (shape->dtype == DSA_BF16_FP8KV && R > 16)
+    return fail(DSA_ERR_UNSUPPORTED, "FP8 keys and values: (H_q/H_kv)*T_q = %d > 16", R);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return fail(DSA_ERR_ALIGNMENT, "q, k, v and out must be non-NULL and 16-byte aligned");
   if (!aligned(kv_len, 4) || !aligned(sel_cnt, 4) || (max_sel > 0 && !aligned(sel_idx, 4)))

@@ -39,9 +39,34 @@ __device__ __forceinline__ void unpack16(const uint4 &u, float *f, float) {
   f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
 }
 
+// Storage tag of FP8 E4M3 key / value rows (one byte per element).
+struct Fp8E4M3 {
+  uint8_t bits;
+};
+
+// One FP8 E4M3 code -> float, exactly.  E4M3 is sign, 4 exponent bits (bias 7) and 3
+// mantissa bits; placed in the top of an fp32's exponent/mantissa fields they read as
+// the same value times 2^-120 (a normal code becomes a normal fp32, a subnormal one a
+// subnormal fp32, both exact), so one multiply by 2^120 restores it.  Inputs are never
+// the NaN code.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const float mag = __uint_as_float((c & 0x7Fu) << 20) * 0x1p120f;
+  return (c & 0x80u) ? -mag : mag;
+}
+
+__device__ __forceinline__ void unpack16(const uint4 &u, float *f, Fp8E4M3) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+#pragma unroll
+    for (int b = 0; b < 4; ++b) f[4 * i + b] = e4m3_to_f32((w[i] >> (8 * b)) & 0xFFu);
+  }
+}
+
 template <typename T> struct Store;
 template <> struct Store<uint16_t> { static constexpr int kPer16 = 8; };
 template <> struct Store<float> { static constexpr int kPer16 = 4; };
+template <> struct Store<Fp8E4M3> { static constexpr int kPer16 = 16; };
 
 // Load N consecutive elements (N * sizeof(T) a multiple of 16, 16-byte aligned) as floats.
 template <typename T, int N>

@@ -16,7 +16,8 @@
 // is contiguous, 2*D bytes).
 // This file holds the split path, for fp32 inputs and for more than 16 query rows
 // per KV head: grid = (split, g, b) writes partials, a second kernel merges them.
-// bf16 with at most 16 rows per KV head takes the tensor-core cluster kernel of
+// bf16 (or bf16 queries over FP8 keys and values) with at most 16 rows per KV head
+// takes the tensor-core cluster kernel of
 // decode_mma.cu.
 #include <math.h>
 
@@ -287,7 +288,7 @@ cudaError_t launch_decode_d(const DecodeArgs &a, cudaStream_t s) {
 
 DecodePlan decode_plan(int B, int H_kv, int R, int D, int dtype, int a_max) {
   DecodePlan p{};
-  if (dtype == 0 && R <= 16) {
+  if ((dtype == DSA_BF16 || dtype == DSA_BF16_FP8KV) && R <= 16) {
     // tensor-core cluster path: up to 16 CTAs per (b, g), whole 16-key sub-tiles each
     constexpr int kSub = 16;
     const int subs = a_max > 0 ? (a_max + kSub - 1) / kSub : 1;

@@ -28,7 +28,18 @@
 //    the CTAs of the cluster merge through distributed shared memory (log-sum-exp
 //    weights; eight threads per output read their CTAs' partials in one round);
 //    nothing goes through HBM but the K/V rows, the query and the output.
+//  * FP8 E4M3 keys and values (a bf16 query, D = 128; the "FP8 KV cache data type" of
+//    the InfiniteHiP summary's throughput runs): a sub-tile is 4 KiB, so up to six are
+//    in flight per warp -- every sub-tile of a 1M-context range at once -- and the
+//    products run as fp16 mma.sync (E4M3 and bf16 values are fp16 values; P rounds to
+//    fp16).  The bytes go from shared memory straight into fragments: Q K^T takes each
+//    16-dim k-step in the order (4t, 4t+1 | 4t+2, 4t+3) for fragment columns
+//    (2t, 2t+1 | 2t+8, 2t+9), so one 32-bit load of four codes is a whole B fragment,
+//    and the sub-tile's key order is permuted the same way (n-tile i, column 2t + e is
+//    key 4t + 2i + e), so the P V fragment of a head dimension is four codes of
+//    consecutive keys.
 #include <cooperative_groups.h>
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include "common.cuh"
@@ -39,10 +50,14 @@
 namespace dsa {
 namespace {
 
-constexpr int kWarps = 4;   // x three ring slots x 8 KiB (d = 128): two CTAs per SM
+// Four warps per CTA: bf16 rows take three ring slots of 8 KiB each (d = 128), FP8 rows
+// up to six of 4 KiB -- about 100 KB either way, two CTAs per SM.  (Eight warps for FP8
+// rows measured slower: at two CTAs per SM the registers then spill.)
+constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kST = 16;      // keys per warp sub-tile
-constexpr int kMaxBuf = 3;   // sub-tiles in flight per warp, at most
+constexpr int kMaxBuf = 3;   // sub-tiles in flight per warp, at most (bf16 rows)
+constexpr int kMaxBuf8 = 6;  // the same for FP8 rows
 constexpr int kTPE = 8;      // threads per output in the cluster merge (C <= 2 * kTPE)
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
@@ -51,11 +66,13 @@ constexpr float kLn2 = 0.6931471805599453f;
 // c ^ (k & 7): the eight rows an ldmatrix reads at one piece index hit eight
 // different bank groups.  The warp and CTA partials reuse the rings once every gather
 // has landed.
-template <int D>
+template <int D, bool FP8 = false>
 struct MmaSmem {
-  static constexpr int kRow = D;                // bf16 per shared row
-  static constexpr int kSlot = 2 * kST * kRow;  // K rows then V rows of one sub-tile
-  __host__ __device__ static size_t ring_bytes(int nbuf) { return static_cast<size_t>(kWarps) * nbuf * kSlot * 2; }
+  static constexpr int kRowBytes = FP8 ? D : 2 * D;      // one key row of one head
+  static constexpr int kSlotBytes = 2 * kST * kRowBytes;   // K rows then V rows of one sub-tile
+  __host__ __device__ static size_t ring_bytes(int nbuf) {
+    return static_cast<size_t>(kWarps) * nbuf * kSlotBytes;
+  }
   __host__ __device__ static size_t part_bytes(int R) {             // warp partials, CTA partial, merge weights
     return (static_cast<size_t>(kWarps + 1) * R * (D + 2) + static_cast<size_t>(kWarps) * R) * 4;
   }
@@ -68,9 +85,10 @@ struct MmaSmem {
 };
 
 // ring slots a warp needs for a range of kps keys (every sub-tile in flight if it fits)
-inline int ring_slots(int kps) {
+inline int ring_slots(int kps, bool fp8) {
+  const int cap = fp8 ? kMaxBuf8 : kMaxBuf;
   const int per_warp = ((kps + kST - 1) / kST + kWarps - 1) / kWarps;
-  return per_warp < 1 ? 1 : (per_warp > kMaxBuf ? kMaxBuf : per_warp);
+  return per_warp < 1 ? 1 : (per_warp > cap ? cap : per_warp);
 }
 
 __device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
@@ -88,17 +106,25 @@ __device__ __forceinline__ float bf16r(float x) {   // x rounded to bf16 (neares
   return __uint_as_float(static_cast<uint32_t>(f32_to_bf16(x)) << 16);
 }
 
-template <int D, int NBUF>
+__device__ __forceinline__ float f16r(float x) {    // x rounded to fp16 (nearest even)
+  return __half2float(__float2half_rn(x));
+}
+
+// byte offset of 16-byte piece c of key row k in a swizzled FP8 tile (128-byte rows)
+__device__ __forceinline__ int sw8_off(int k, int c) { return k * 128 + ((c ^ (k & 7)) << 4); }
+
+template <int D, int NBUF, bool FP8>
 __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   namespace cg = cooperative_groups;
-  using SM = MmaSmem<D>;
+  using SM = MmaSmem<D, FP8>;
+  static_assert(!FP8 || D == 128, "FP8 rows: D = 128");
   constexpr int KS = D / 16;   // k-steps of Q K^T
   constexpr int NT = D / 8;    // n-tiles of P V
-  constexpr int CH = D / 8;    // 16-byte pieces per K or V row
+  constexpr int CH = SM::kRowBytes / 16;   // 16-byte pieces per K or V row
   extern __shared__ __align__(16) unsigned char smem[];
   const int G = a.H_q / a.H_kv;
   const int R = G * a.T_q;     // <= 16
-  uint16_t *ring = reinterpret_cast<uint16_t *>(smem);
+  unsigned char *ring = smem;
   float *s_part = reinterpret_cast<float *>(smem);   // over the drained rings
   int *s_pos = reinterpret_cast<int *>(smem + SM::rings_or_parts(NBUF, R));
 
@@ -117,14 +143,20 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
     auto qpair = [&](int r, int d) -> uint32_t {
       if (r >= R) return 0u;
       const int t = r / G, h = g * G + (r - t * G);
-      return *reinterpret_cast<const uint32_t *>(q + ((static_cast<size_t>(b) * a.T_q + t) * a.H_q + h) * D + d);
+      const uint32_t w = *reinterpret_cast<const uint32_t *>(
+          q + ((static_cast<size_t>(b) * a.T_q + t) * a.H_q + h) * D + d);
+      if constexpr (FP8) return pack_f16x2(bf16_lo(w), bf16_hi(w));   // exact but for tiny values
+      else return w;
     };
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      qa[ks][0] = qpair(gq, ks * 16 + 2 * tq);
-      qa[ks][1] = qpair(gq + 8, ks * 16 + 2 * tq);
-      qa[ks][2] = qpair(gq, ks * 16 + 8 + 2 * tq);
-      qa[ks][3] = qpair(gq + 8, ks * 16 + 8 + 2 * tq);
+      // FP8: fragment columns (2t, 2t+1 | 2t+8, 2t+9) hold dims (4t, 4t+1 | 4t+2, 4t+3)
+      const int d0 = FP8 ? ks * 16 + 4 * tq : ks * 16 + 2 * tq;
+      const int d1 = FP8 ? d0 + 2 : d0 + 8;
+      qa[ks][0] = qpair(gq, d0);
+      qa[ks][1] = qpair(gq + 8, d0);
+      qa[ks][2] = qpair(gq, d1);
+      qa[ks][3] = qpair(gq + 8, d1);
     }
   }
   const int32_t *sel = a.sel_idx + static_cast<size_t>(b) * a.max_sel;
@@ -147,11 +179,12 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   const int a_len = n_s + cnt + n_w;
   const int k_end = min(a_len, k_begin + a.keys_per_split);
   const int n_sub = k_end > k_begin ? (k_end - k_begin + kST - 1) / kST : 0;
-  const uint16_t *kbase = static_cast<const uint16_t *>(a.k) +
-                          static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D;
-  const uint16_t *vbase = static_cast<const uint16_t *>(a.v) +
-                          static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D;
-  const size_t row_stride = static_cast<size_t>(a.H_kv) * D;
+  constexpr int kEl = FP8 ? 1 : 2;   // bytes per K / V element
+  const unsigned char *kbase = static_cast<const unsigned char *>(a.k) +
+                               (static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D) * kEl;
+  const unsigned char *vbase = static_cast<const unsigned char *>(a.v) +
+                               (static_cast<size_t>(b) * a.T_max * a.H_kv * D + static_cast<size_t>(g) * D) * kEl;
+  const size_t row_stride = static_cast<size_t>(a.H_kv) * D * kEl;   // bytes
   const float sl2 = a.scale * kLog2e;
 
   // every key position of this CTA's range (-1: none)
@@ -177,22 +210,23 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   }
   __syncthreads();
 
-  uint16_t *wring = ring + warp * NBUF * SM::kSlot;
+  unsigned char *wring = ring + warp * NBUF * SM::kSlotBytes;
   // sub-tile j of the CTA range -> ring slot `slot` (one commit group per call)
   auto issue = [&](int j, int slot) {
     if (j < n_sub) {
-      uint16_t *sk = wring + slot * SM::kSlot;
-      uint16_t *sv = sk + kST * SM::kRow;
+      unsigned char *sk = wring + slot * SM::kSlotBytes;
+      unsigned char *sv = sk + kST * SM::kRowBytes;
       const int *pj = s_pos + j * kST;
 #pragma unroll
       for (int e = lane; e < kST * CH; e += 32) {
         const int key = e / CH, c = e - key * CH;
         const int pos = pj[key];
-        uint16_t *dk = sk + sw_off<D>(key, c);
-        uint16_t *dv = sv + sw_off<D>(key, c);
+        const int off = FP8 ? sw8_off(key, c) : 2 * sw_off<D>(key, c);
+        unsigned char *dk = sk + off;
+        unsigned char *dv = sv + off;
         if (pos >= 0) {
-          cp_async16(dk, kbase + static_cast<size_t>(pos) * row_stride + c * 8);
-          cp_async16(dv, vbase + static_cast<size_t>(pos) * row_stride + c * 8);
+          cp_async16(dk, kbase + static_cast<size_t>(pos) * row_stride + c * 16);
+          cp_async16(dv, vbase + static_cast<size_t>(pos) * row_stride + c * 16);
         } else {
           *reinterpret_cast<uint4 *>(dk) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4 *>(dv) = make_uint4(0, 0, 0, 0);
@@ -213,17 +247,30 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
     const int slot = it % NBUF;
     asm volatile("cp.async.wait_group %0;\n" ::"n"(NBUF - 1) : "memory");
     __syncwarp();
-    const uint16_t *sk = wring + slot * SM::kSlot;
-    const uint16_t *sv = sk + kST * SM::kRow;
+    const unsigned char *sk = wring + slot * SM::kSlotBytes;
+    const unsigned char *sv = sk + kST * SM::kRowBytes;
     // S = Q K^T: two n-tiles of 8 keys
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
+    if constexpr (FP8) {
+      // n-tile i, column gq holds key 4 (gq >> 1) + (gq & 1) + 2i; one 32-bit load gives
+      // that key's dims (4t .. 4t+3) of k-step ks: b0 = the first two, b1 = the last two
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const int key = 4 * (gq >> 1) + (gq & 1) + 2 * nt;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint32_t w = *reinterpret_cast<const uint32_t *>(sk + sw8_off(key, ks) + 4 * tq);
+          mma_16816_f16(s[nt], qa[ks], e4m3x2_to_f16x2(w), e4m3x2_to_f16x2(w >> 16));
+        }
+      }
+    } else {
       const int mtx = lane >> 3, rr = lane & 7;
       const int key = (mtx >> 1) * 8 + rr;
+      const uint16_t *sk16 = reinterpret_cast<const uint16_t *>(sk);
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         uint32_t bk[4];
-        ldsm_x4(bk, sk + sw_off<D>(key, 2 * ks + (mtx & 1)));
+        ldsm_x4(bk, sk16 + sw_off<D>(key, 2 * ks + (mtx & 1)));
         mma_16816(s[0], qa[ks], bk[0], bk[1]);
         mma_16816(s[1], qa[ks], bk[2], bk[3]);
       }
@@ -235,7 +282,7 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int key = nt * 8 + 2 * tq + (e & 1);
+        const int key = FP8 ? 4 * tq + 2 * nt + (e & 1) : nt * 8 + 2 * tq + (e & 1);
         const float v = pj[key] >= 0 ? s[nt][e] * sl2 : -INFINITY;
         s[nt][e] = v;
         if (e < 2) mx0 = fmaxf(mx0, v);
@@ -251,19 +298,22 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
     const float al1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - n1);
     m0 = n0;
     m1 = n1;
-    // probabilities, rounded to bf16 once: the same values feed P V and the row sums
+    // probabilities, rounded once to the operand type (bf16, or fp16 with FP8 rows): the
+    // same values feed P V and the row sums
+    auto rnd = [](float x) { return FP8 ? f16r(x) : bf16r(x); };
+    auto pack = [](float lo, float hi) { return FP8 ? pack_f16x2(lo, hi) : pack_bf16x2(lo, hi); };
     uint32_t pa[4];
     float ps0 = 0.f, ps1 = 0.f;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
-      const float p0 = n0 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][0] - n0));
-      const float p1 = n0 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][1] - n0));
-      const float p2 = n1 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][2] - n1));
-      const float p3 = n1 == -INFINITY ? 0.f : bf16r(exp2f(s[nt][3] - n1));
+      const float p0 = n0 == -INFINITY ? 0.f : rnd(exp2f(s[nt][0] - n0));
+      const float p1 = n0 == -INFINITY ? 0.f : rnd(exp2f(s[nt][1] - n0));
+      const float p2 = n1 == -INFINITY ? 0.f : rnd(exp2f(s[nt][2] - n1));
+      const float p3 = n1 == -INFINITY ? 0.f : rnd(exp2f(s[nt][3] - n1));
       ps0 += p0 + p1;
       ps1 += p2 + p3;
-      pa[2 * nt] = pack_bf16x2(p0, p1);       // a0 (n-tile 0) / a2 (n-tile 1): row gq
-      pa[2 * nt + 1] = pack_bf16x2(p2, p3);   // a1 / a3: row gq + 8
+      pa[2 * nt] = pack(p0, p1);       // a0 (n-tile 0) / a2 (n-tile 1): row gq
+      pa[2 * nt + 1] = pack(p2, p3);   // a1 / a3: row gq + 8
     }
     ps0 += __shfl_xor_sync(kFull, ps0, 1);
     ps0 += __shfl_xor_sync(kFull, ps0, 2);
@@ -279,14 +329,27 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
       o[i][3] *= al1;
     }
     // O += P V: V rows (keys) are the K side, head dimensions the N side
-    {
-      const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
+    const uint32_t pfrag[4] = {pa[0], pa[1], pa[2], pa[3]};
+    if constexpr (FP8) {
+      // fragment rows (2t, 2t+1 | 2t+8, 2t+9) are keys 4t .. 4t+3; column gq of n-tile i is
+      // head dim 8i + gq: four codes, one per key
+#pragma unroll
+      for (int i = 0; i < NT; ++i) {
+        const int d = 8 * i + gq;
+        uint32_t x[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) x[u] = sv[sw8_off(4 * tq + u, d >> 4) + (d & 15)];
+        mma_16816_f16(o[i], pfrag, e4m3x2_to_f16x2(x[0] | (x[1] << 8)),
+                      e4m3x2_to_f16x2(x[2] | (x[3] << 8)));
+      }
+    } else {
       const int mtx = lane >> 3, rr = lane & 7;
       const int key = (mtx & 1) * 8 + rr;
+      const uint16_t *sv16 = reinterpret_cast<const uint16_t *>(sv);
 #pragma unroll
       for (int dp = 0; dp < D / 16; ++dp) {
         uint32_t bv[4];
-        ldsm_x4_trans(bv, sv + sw_off<D>(key, 2 * dp + (mtx >> 1)));
+        ldsm_x4_trans(bv, sv16 + sw_off<D>(key, 2 * dp + (mtx >> 1)));
         mma_16816(o[2 * dp], pfrag, bv[0], bv[1]);
         mma_16816(o[2 * dp + 1], pfrag, bv[2], bv[3]);
       }
@@ -404,18 +467,30 @@ __global__ void __launch_bounds__(kThreads) decode_mma_kernel(DecodeArgs a) {
   cluster.sync();   // keep this CTA's shared memory until every reader is done
 }
 
-template <int D>
+template <int D, bool FP8>
 cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
   DecodeArgs a = a0;
+  using SM = MmaSmem<D, FP8>;
   const int R = (a.H_q / a.H_kv) * a.T_q;
   const int keys = a.n_split * a.keys_per_split;
   auto kernel_for = [](int nbuf) {
-    return nbuf == 1 ? decode_mma_kernel<D, 1> : nbuf == 2 ? decode_mma_kernel<D, 2>
-                                                           : decode_mma_kernel<D, 3>;
+    if constexpr (FP8) {
+      switch (nbuf) {
+        case 1: return decode_mma_kernel<D, 1, true>;
+        case 2: return decode_mma_kernel<D, 2, true>;
+        case 3: return decode_mma_kernel<D, 3, true>;
+        case 4: return decode_mma_kernel<D, 4, true>;
+        case 5: return decode_mma_kernel<D, 5, true>;
+        default: return decode_mma_kernel<D, 6, true>;
+      }
+    } else {
+      return nbuf == 1 ? decode_mma_kernel<D, 1, false>
+                       : nbuf == 2 ? decode_mma_kernel<D, 2, false> : decode_mma_kernel<D, 3, false>;
+    }
   };
-  int nbuf = ring_slots(a.keys_per_split);
+  int nbuf = ring_slots(a.keys_per_split, FP8);
   auto kern = kernel_for(nbuf);
-  size_t smem = MmaSmem<D>::bytes(a.keys_per_split, R, nbuf);
+  size_t smem = SM::bytes(a.keys_per_split, R, nbuf);
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   if (a.n_split > 8) {
@@ -444,9 +519,9 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
       (void)cudaGetLastError();
       a.n_split = 8;
       a.keys_per_split = ((keys / 8 + kST - 1) / kST) * kST;
-      nbuf = ring_slots(a.keys_per_split);
+      nbuf = ring_slots(a.keys_per_split, FP8);
       kern = kernel_for(nbuf);
-      smem = MmaSmem<D>::bytes(a.keys_per_split, R, nbuf);
+      smem = SM::bytes(a.keys_per_split, R, nbuf);
       e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
       if (e != cudaSuccess) return e;
       cfg.gridDim.x = 8;
@@ -456,7 +531,7 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
   }
   cfg.numAttrs = 2;
   {
-    ProfScope ps("decode_cluster_mma", s);
+    ProfScope ps(FP8 ? "decode_cluster_mma_fp8" : "decode_cluster_mma", s);
     e = cudaLaunchKernelEx(&cfg, kern, a);
   }
   return e;
@@ -465,7 +540,8 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_decode_mma(const DecodeArgs &a, cudaStream_t s) {
-  return a.D == 128 ? launch_mma_d<128>(a, s) : launch_mma_d<64>(a, s);
+  if (a.dtype == DSA_BF16_FP8KV) return launch_mma_d<128, true>(a, s);   // D = 128 checked by the API
+  return a.D == 128 ? launch_mma_d<128, false>(a, s) : launch_mma_d<64, false>(a, s);
 }
 
 }  // namespace dsa

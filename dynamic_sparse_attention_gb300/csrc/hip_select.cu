@@ -57,7 +57,9 @@ __host__ __device__ inline size_t score_smem_q_off(bool explicit_list, int L) {
 // NT_MAX / MIN_B: launch bounds.  Up to 32 query heads (256 threads) the kernel keeps
 // eight CTAs (64 warps) resident per SM: every octet waits on one dependent key row at
 // a time, so the number of tournaments in flight is what feeds HBM.
-template <typename T, int D, bool QREG, int NT_MAX, int MIN_B>
+// TQ / TK: storage of the query (bf16 or fp32) and of the key rows (the same, or FP8
+// E4M3 under a bf16 query).
+template <typename TQ, typename TK, int D, bool QREG, int NT_MAX, int MIN_B>
 __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreArgs a) {
   constexpr int EPL = D / 8;
   extern __shared__ __align__(16) unsigned char smem[];
@@ -73,14 +75,14 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
   if (j >= n_chunk) return;
   const int base = j * a.L;
   const int len = min(a.L, ir.n_in - base);
-  const T *q = static_cast<const T *>(a.q) + static_cast<size_t>(b) * a.T_q * a.H_q * D;
+  const TQ *q = static_cast<const TQ *>(a.q) + static_cast<size_t>(b) * a.T_q * a.H_q * D;
   if (ir.in) {   // a cached list may be stale: never read outside the key rows
     for (int x = threadIdx.x; x < len; x += blockDim.x) s_pos[x] = min(max(ir.in[base + x], 0), a.T_max - 1);
   }
   if (!QREG) {
     const int n = a.T_q * a.H_q * D;
     for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      if constexpr (sizeof(T) == 2) s_q[e] = bf16_to_f32(reinterpret_cast<const uint16_t *>(q)[e]);
+      if constexpr (sizeof(TQ) == 2) s_q[e] = bf16_to_f32(reinterpret_cast<const uint16_t *>(q)[e]);
       else s_q[e] = reinterpret_cast<const float *>(q)[e];
     }
   }
@@ -91,16 +93,18 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
   if (h < a.H_q) {
     const int g = h / G;
     const unsigned omask = 0xffu << (threadIdx.x & 24);
-    constexpr int NV = EPL * static_cast<int>(sizeof(T)) / 16;   // 16-byte loads per lane
+    constexpr int NV = EPL * static_cast<int>(sizeof(TK)) / 16;    // 16-byte key loads per lane
+    constexpr int NVQ = EPL * static_cast<int>(sizeof(TQ)) / 16;   // and query loads
+    static_assert(NV >= 1, "a lane's key slice is at least 16 bytes");
     // the query slice stays in its storage format too (bf16 pairs or fp32)
-    uint4 qraw[QREG ? NV : 1];
+    uint4 qraw[QREG ? NVQ : 1];
     if (QREG) {
       const uint4 *qp = reinterpret_cast<const uint4 *>(q + static_cast<size_t>(h) * D + sub * EPL);
 #pragma unroll
-      for (int i = 0; i < NV; ++i) qraw[i] = __ldg(qp + i);
+      for (int i = 0; i < NVQ; ++i) qraw[i] = __ldg(qp + i);
     }
-    const T *kb = static_cast<const T *>(a.k) + static_cast<size_t>(b) * a.T_max * a.H_kv * D +
-                  static_cast<size_t>(g) * D + sub * EPL;
+    const TK *kb = static_cast<const TK *>(a.k) + static_cast<size_t>(b) * a.T_max * a.H_kv * D +
+                   static_cast<size_t>(g) * D + sub * EPL;
     const size_t row_stride = static_cast<size_t>(a.H_kv) * D;
     const int T_q = QREG ? 1 : a.T_q;
     auto pos_of = [&](int x) -> int { return ir.in ? s_pos[x] : ir.start + base + x; };
@@ -114,14 +118,41 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
       for (int t = 0; t < T_q; ++t) {
         const float *qq = s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
         float d = 0.f;
-        constexpr int per = Store<T>::kPer16;
+        if constexpr (std::is_same<TQ, TK>::value) {
+          constexpr int per = Store<TK>::kPer16;
 #pragma unroll
-        for (int i = 0; i < NV; ++i) {
-          float kf[per], qf[per];
-          unpack16(raw[i], kf, T());
-          if (QREG) unpack16(qraw[i], qf, T());
+          for (int i = 0; i < NV; ++i) {
+            float kf[per], qf[per];
+            unpack16(raw[i], kf, TK());
+            if (QREG) unpack16(qraw[i], qf, TQ());
 #pragma unroll
-          for (int e = 0; e < per; ++e) d = fmaf(QREG ? qf[e] : qq[i * per + e], kf[e], d);
+            for (int e = 0; e < per; ++e) d = fmaf(QREG ? qf[e] : qq[i * per + e], kf[e], d);
+          }
+        } else {
+          // FP8 keys under a bf16 query: each 32-bit key word is four elements, matched by
+          // two 32-bit query words
+#pragma unroll
+          for (int i = 0; i < NV; ++i) {
+            const uint32_t kw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+            for (int wi = 0; wi < 4; ++wi) {
+              const int e0 = 16 * i + 4 * wi;   // first element of this word in the slice
+#pragma unroll
+              for (int bb = 0; bb < 4; ++bb) {
+                const float kf = e4m3_to_f32((kw[wi] >> (8 * bb)) & 0xFFu);
+                float qf;
+                if (QREG) {
+                  const uint4 &qv = qraw[(e0 + bb) >> 3];
+                  const int qw = ((e0 + bb) >> 1) & 3;
+                  const uint32_t word = qw == 0 ? qv.x : qw == 1 ? qv.y : qw == 2 ? qv.z : qv.w;
+                  qf = ((e0 + bb) & 1) ? bf16_hi(word) : bf16_lo(word);
+                } else {
+                  qf = qq[e0 + bb];
+                }
+                d = fmaf(qf, kf, d);
+              }
+            }
+          }
         }
         d += __shfl_xor_sync(omask, d, 4);
         d += __shfl_xor_sync(omask, d, 2);
@@ -549,7 +580,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
   }
 }
 
-template <typename T, int D>
+template <typename TQ, typename TK, int D>
 cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
   const bool explicit_list = a.in_idx != nullptr;
   const bool qreg = a.T_q == 1;
@@ -563,19 +594,22 @@ cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
     launch_pdl(kern, grid, dim3(threads), smem, s, a);
   };
   // fp32 rows need twice the registers: six CTAs per SM there
-  if (qreg && threads <= 256) go(stage_score_kernel<T, D, true, 256, sizeof(T) == 2 ? 8 : 6>);
-  else if (qreg) go(stage_score_kernel<T, D, true, 1024, 1>);
-  else go(stage_score_kernel<T, D, false, 1024, 1>);
+  constexpr int kMinB = sizeof(TQ) == 2 ? 8 : 6;
+  if (qreg && threads <= 256) go(stage_score_kernel<TQ, TK, D, true, 256, kMinB>);
+  else if (qreg) go(stage_score_kernel<TQ, TK, D, true, 1024, 1>);
+  else go(stage_score_kernel<TQ, TK, D, false, 1024, 1>);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_stage_score(const StageScoreArgs &a, cudaStream_t s) {
-  if (a.dtype == 0) {
-    return a.D == 128 ? launch_score_t<uint16_t, 128>(a, s) : launch_score_t<uint16_t, 64>(a, s);
+  if (a.dtype == DSA_BF16_FP8KV) return launch_score_t<uint16_t, Fp8E4M3, 128>(a, s);   // D = 128
+  if (a.dtype == DSA_BF16) {
+    return a.D == 128 ? launch_score_t<uint16_t, uint16_t, 128>(a, s)
+                      : launch_score_t<uint16_t, uint16_t, 64>(a, s);
   }
-  return a.D == 128 ? launch_score_t<float, 128>(a, s) : launch_score_t<float, 64>(a, s);
+  return a.D == 128 ? launch_score_t<float, float, 128>(a, s) : launch_score_t<float, float, 64>(a, s);
 }
 
 cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s) {

@@ -6,6 +6,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "dsa.h"
+
 namespace dsa {
 
 // Launch with programmatic stream serialization allowed: the grid may start while

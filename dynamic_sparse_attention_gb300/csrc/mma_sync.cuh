@@ -1,4 +1,4 @@
-// Warp-level bf16 MMA helpers (mma.sync m16n8k16, ldmatrix, cp.async).
+// Warp-level bf16 / fp16 MMA helpers (mma.sync m16n8k16, ldmatrix, cp.async).
 //
 // Fragment layouts (g = lane / 4, t = lane % 4):
 //   A 16x16 (row-major): a0 = (g, 2t..2t+1), a1 = (g+8, 2t..), a2 = (g, 2t+8..), a3 = (g+8, 2t+8..)
@@ -17,6 +17,31 @@ __device__ __forceinline__ void mma_16816(float *c, const uint32_t *a, uint32_t 
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// the same with fp16 operands (A and B both f16)
+__device__ __forceinline__ void mma_16816_f16(float *c, const uint32_t *a, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// two floats -> packed f16x2 (lo in the low half), round to nearest even
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// two FP8 E4M3 codes (first in the low byte) -> f16x2 (first in the low half); exact,
+// every E4M3 value is an fp16 value
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
+  uint32_t r;
+  const uint16_t h = static_cast<uint16_t>(x);
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;\n" : "=r"(r) : "h"(h));
+  return r;
 }
 
 __device__ __forceinline__ unsigned smem_addr(const void *p) {

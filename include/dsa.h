@@ -56,7 +56,16 @@ typedef enum {
   DSA_ERR_DEVICE_CHECK = -6  /* reserved for device-side checks */
 } dsa_status;
 
-typedef enum { DSA_BF16 = 0, DSA_F32 = 1 } dsa_dtype;
+/* Element types of q / k / v (out has the type of q):
+ *   DSA_BF16        bf16 q, k, v (raw bit patterns)
+ *   DSA_F32         fp32 q, k, v
+ *   DSA_BF16_FP8KV  bf16 q; k and v FP8 E4M3 codes, one byte per element (OCP E4M3:
+ *                   bias 7, no infinity, S.1111.111 NaN); D = 128 and at most 16 query
+ *                   rows per KV head ((H_q/H_kv) * T_q <= 16).  The InfiniteHiP
+ *                   summary's throughput runs store the KV cache in this type.  A
+ *                   per-tensor scale is the caller's: fold k's scale into `scale` and
+ *                   multiply out by v's (lse then refers to the rescaled scores). */
+typedef enum { DSA_BF16 = 0, DSA_F32 = 1, DSA_BF16_FP8KV = 2 } dsa_dtype;
 
 /* ------------------------------------------------------------------ decode */
 
@@ -65,7 +74,7 @@ typedef enum { DSA_BF16 = 0, DSA_F32 = 1 } dsa_dtype;
  *   k, v   [B, T_max, H_kv, D] the resident KV cache; row t of batch b is valid
  *                              for t < kv_len[b]
  * H_q % H_kv == 0; query head h reads KV head h / (H_q / H_kv).
- * D in {64, 128}; dtype DSA_BF16 (raw bf16) or DSA_F32. */
+ * D in {64, 128}; dtype one of dsa_dtype (DSA_BF16_FP8KV: D = 128 only). */
 typedef struct {
   int B, T_max, T_q, H_q, H_kv, D;
   int dtype;

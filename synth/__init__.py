@@ -8,6 +8,8 @@ from .workloads import (  # noqa: F401
     DecodeCase,
     PrefillCase,
     f32_to_bf16_bits,
+    f32_to_e4m3_bits,
+    with_fp8_kv,
     decode_case,
     decode_steps,
     prefill_case,

@@ -26,6 +26,31 @@ def f32_to_bf16_bits(x: np.ndarray) -> np.ndarray:
     return ((u + bias) >> 16).astype(np.uint16)
 
 
+def f32_to_e4m3_bits(x: np.ndarray) -> np.ndarray:
+    """Round fp32 values to FP8 E4M3 (nearest, ties to even, saturating at +-448);
+    return uint8 codes.  Positive codes grow with the value (code = 8 * biased exponent
+    + mantissa, subnormals m * 2^-9 below 2^-6), so the rounding is done on the code."""
+    x = np.asarray(x, dtype=np.float32)
+    a = np.abs(x).astype(np.float64)
+    _, ex = np.frexp(np.maximum(a, 2.0 ** -6))
+    E = ex.astype(np.int64) - 1                       # floor(log2 a) for a >= 2^-6
+    normal = np.rint(a / np.exp2(E - 3.0)).astype(np.int64) + 8 * E + 48
+    sub = np.rint(a * 512.0).astype(np.int64)         # a < 2^-6: multiples of 2^-9
+    code = np.where(a < 2.0 ** -6, sub, normal)
+    code = np.minimum(code, 126)
+    return (code | (np.signbit(x).astype(np.int64) << 7)).astype(np.uint8)
+
+
+def with_fp8_kv(case: "DecodeCase") -> "DecodeCase":
+    """The same decode case with its keys and values stored as FP8 E4M3 (rounded from
+    their bf16 / fp32 values); the queries keep their type."""
+    from dataclasses import replace
+    src = case.dtype == "bf16"
+    k = f32_to_e4m3_bits(_as_f32(case.k, src))
+    v = f32_to_e4m3_bits(_as_f32(case.v, src))
+    return replace(case, name=case.name + "_fp8kv", k=k, v=v, kv_dtype="e4m3")
+
+
 def _normal_bits(rng: np.random.Generator, shape, bf16: bool) -> np.ndarray:
     """Draw N(0,1) fp32 in fixed-size pieces; bf16 bits or fp32 values."""
     n = int(np.prod(shape))
@@ -68,6 +93,12 @@ class DecodeCase:
     k: np.ndarray                  # [B, T_max, H_kv, D]
     v: np.ndarray                  # [B, T_max, H_kv, D]
     planted: list = field(default_factory=list)  # per batch row: planted key positions
+    kv_dtype: str = ""             # "" (as dtype) or "e4m3" (uint8 codes) for k and v
+
+    @property
+    def kvd(self) -> str:
+        """Storage type of k and v."""
+        return self.kv_dtype or self.dtype
 
     @property
     def G(self) -> int:

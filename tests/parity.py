@@ -23,7 +23,10 @@ REL_BAND = 1e-3
 
 
 def to_dev(a: np.ndarray, dtype: str) -> torch.Tensor:
-    """Stored bit patterns -> CUDA tensor of the matching torch dtype."""
+    """Stored bit patterns -> CUDA tensor of the matching torch dtype (FP8 E4M3 codes
+    travel as uint8: the library reads the bytes)."""
+    if dtype == "e4m3":
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.uint8)).cuda()
     if dtype == "bf16":
         return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).view(torch.bfloat16).cuda()
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).cuda()
@@ -136,7 +139,7 @@ def check_hip_stage(case, b, dbg, i, I, stats):
     reps = dbg["rep"][i][b, :, :n].cpu().numpy().astype(np.int64)
     rho = dbg["rep_score"][i][b, :, :n].cpu().numpy()
     s_gpu = dbg["chunk_score"][i][b, :n].cpu().numpy()
-    rho64, flips = check_tournament(q64, case.k[b], case.dtype, chunks, reps, rho, case.G, case.D)
+    rho64, flips = check_tournament(q64, case.k[b], case.kvd, chunks, reps, rho, case.G, case.D)
     stats["flips"] += flips
     assert np.array_equal(s_gpu, rho.max(axis=0)), "chunk score is not the max over heads"
     s64 = rho64.max(axis=0)

@@ -199,3 +199,20 @@ def test_mixed_patterns_validate_arguments(lib):
     big = _pshape(H_q=512, H_kv=8)
     c, keep = cfg([1] * 512)
     assert lib.mixed_index_build_workspace(ctypes.byref(big), ctypes.byref(c), ctypes.byref(n)) == -2
+
+
+def test_fp8_kv_shapes(lib):
+    n = ctypes.c_size_t()
+    c = _cfg()
+    # bf16 queries over FP8 keys / values: D = 128 only, at most 16 rows per KV head
+    s = _shape(dtype=2)
+    assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == 0
+    assert lib.sparse_attn_decode_workspace(ctypes.byref(s), 4096, 128, 1024, ctypes.byref(n)) == 0
+    assert n.value == 0                        # the cluster kernel needs no scratch
+    s = _shape(dtype=2, D=64)
+    assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == -2
+    s = _shape(dtype=2, T_q=8)                 # 4 heads per KV head x 8 rows = 32 > 16
+    assert lib.sparse_attn_decode_workspace(ctypes.byref(s), 4096, 128, 1024, ctypes.byref(n)) == -2
+    assert b"FP8" in lib.dsa_last_error()
+    s = _shape(dtype=3)
+    assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == -2

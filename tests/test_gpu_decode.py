@@ -10,7 +10,7 @@ from dynamic_sparse_attention_gb300 import _build
 from oracle import hip
 from oracle.numerics import to_f64
 from parity import attention_errors, check_hip_row, check_hip_stage, from_dev_bits, to_dev
-from synth import decode_128k, decode_batch16, decode_case, decode_steps, decode_tiny
+from synth import decode_128k, decode_batch16, decode_case, decode_steps, decode_tiny, with_fp8_kv
 
 pytestmark = pytest.mark.gpu
 
@@ -26,8 +26,8 @@ def _lib():
 
 def _run(case):
     q = to_dev(case.q, case.dtype)
-    k = to_dev(case.k, case.dtype)
-    v = to_dev(case.v, case.dtype)
+    k = to_dev(case.k, case.kvd)
+    v = to_dev(case.v, case.kvd)
     kv_len = torch.from_numpy(case.kv_len).cuda()
     cfg = dsa.HipConfig(case.chunk, case.keep, case.n_sink, case.n_stream)
     sel_idx, sel_cnt, dbg = dsa.hip_select(q, k, kv_len, cfg, debug=True)
@@ -49,7 +49,7 @@ def _check_case(case, rows=None):
         T = int(case.kv_len[b])
         A = hip.attended_set(T, case.n_sink, case.n_stream, I)
         q64 = to_f64(case.q[b], case.dtype)
-        O64, lse64 = hip.decode_attention(q64, case.k[b], case.v[b], case.dtype, A, case.scale,
+        O64, lse64 = hip.decode_attention(q64, case.k[b], case.v[b], case.kvd, A, case.scale,
                                           case.G)
         mx, mn = attention_errors(o_gpu[b], O64)
         assert mx <= MAX_ABS and mn <= MEAN_ABS, f"row {b}: max {mx:.3e} mean {mn:.3e}"
@@ -273,3 +273,45 @@ def test_cached_lists_are_clamped_to_the_key_rows():
     assert dsa.device_error() == 0
     assert ((cnt >= 0) & (cnt <= c.keep[-1])).all()
     assert torch.isfinite(o.float()).all()
+
+
+# ------------------------------------------------------------ FP8 E4M3 keys and values
+
+def test_fp8_kv_small_ragged():
+    """bf16 queries over FP8 E4M3 keys and values: selection replayed against the oracle
+    on the decoded keys, attention against the fp64 oracle (ragged batch, partial chunks)."""
+    c = with_fp8_kv(decode_case("ragged", B=3, T=5000, T_q=1, H_q=8, H_kv=2, D=128,
+                                dtype="bf16", chunk=(64, 16, 4), keep=(1024, 256, 64), n_sink=13,
+                                n_stream=100, seed=31, plant="uniform", n_plant=16,
+                                kv_len=[5000, 3333, 1210]))
+    assert c.k.dtype == np.uint8 and c.kvd == "e4m3"
+    _check_case(c)
+
+
+def test_fp8_kv_sixteen_rows_per_kv_head():
+    c = with_fp8_kv(decode_case("block", B=2, T=3000, T_q=4, H_q=8, H_kv=2, D=128, dtype="bf16",
+                                chunk=(32, 8), keep=(512, 128), n_sink=8, n_stream=32, seed=39,
+                                plant="none", kv_len=[3000, 2001]))
+    _check_case(c)
+
+
+def test_fp8_kv_128k_config():
+    """The 128K GQA workload with its keys and values rounded to FP8 E4M3."""
+    _check_case(with_fp8_kv(decode_128k()))
+
+
+def test_fp8_kv_matches_float8_tensors():
+    """A float8_e4m3fn tensor and a uint8 tensor of the same codes give the same results."""
+    c = with_fp8_kv(decode_case("f8", B=1, T=2000, T_q=1, H_q=4, H_kv=1, D=128, dtype="bf16",
+                                chunk=(32, 8), keep=(256, 64), n_sink=4, n_stream=16, seed=40))
+    q = to_dev(c.q, "bf16")
+    k8, v8 = to_dev(c.k, "e4m3"), to_dev(c.v, "e4m3")
+    kv_len = torch.from_numpy(c.kv_len).cuda()
+    cfg = dsa.HipConfig(c.chunk, c.keep, c.n_sink, c.n_stream)
+    s1, n1 = dsa.hip_select(q, k8, kv_len, cfg)
+    o1, _ = dsa.sparse_attn_decode(q, k8, v8, kv_len, s1, n1, n_sink=4, n_stream=16)
+    kf, vf = k8.view(torch.float8_e4m3fn), v8.view(torch.float8_e4m3fn)
+    s2, n2 = dsa.hip_select(q, kf, kv_len, cfg)
+    o2, _ = dsa.sparse_attn_decode(q, kf, vf, kv_len, s2, n2, n_sink=4, n_stream=16)
+    torch.cuda.synchronize()
+    assert torch.equal(s1, s2) and torch.equal(n1, n2) and torch.equal(o1, o2)

@@ -349,3 +349,19 @@ def test_stale_stage0_list_and_the_attended_set():
         left = np.arange(T0 - c.n_stream, T - c.n_stream)
         assert not np.isin(left, A).any()
         assert (0 in ran) == (step % 8 == 0)
+
+
+# ------------------------------------------------------------ FP8 E4M3 keys and values
+
+def test_e4m3_decoding_matches_torch_float8():
+    """Every one of the 256 codes against torch's float8_e4m3fn view (NaN codes too)."""
+    from oracle.numerics import e4m3_to_f64
+    codes = np.arange(256, dtype=np.uint8)
+    got = e4m3_to_f64(codes)
+    want = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(np.isnan(got), np.isnan(want)) and np.isnan(got).sum() == 2
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+    # the format's landmarks: largest finite 448, smallest subnormal 2^-9, smallest normal 2^-6
+    assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
+    assert got[0xFE] == -448.0 and got[0x80] == 0.0
