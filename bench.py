@@ -42,7 +42,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # finest stage refreshed together with the third
 CACHE_PRESETS = {"default": (16, 8, 4, 4), "flash": (96, 24, 8, 8)}
 NCU_TRAFFIC = {
-    ("hip_stage_score_s0", "decode_gqa_T1048576"): 200670720 + 5314560,
+    ("hip_stage_score_s0", "decode_gqa_T1048576"): 201646080 + 5499648,
     ("prefill_attention_tc", "prefill_vs_S131072"): 4348859392 + 1075625472,
 }
 

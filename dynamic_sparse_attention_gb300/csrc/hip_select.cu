@@ -54,6 +54,9 @@ __host__ __device__ inline size_t score_smem_q_off(bool explicit_list, int L) {
   return o;
 }
 
+// tournament levels whose candidate rows are requested from L2 ahead of time
+constexpr int kWarmLevels = 2;
+
 // NT_MAX / MIN_B: launch bounds.  Up to 32 query heads (256 threads) the kernel keeps
 // eight CTAs (64 warps) resident per SM: every octet waits on one dependent key row at
 // a time, so the number of tournaments in flight is what feeds HBM.
@@ -161,6 +164,36 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
       }
       return best;
     };
+    // The first kWarmLevels probes of every head's tournament can only be one of the
+    // 2^level - 1 midpoints of the first levels (the same for every head of the chunk):
+    // ask L2 for those rows now, in the round of the first load, so those levels' loads
+    // hit L2 instead of each waiting a DRAM round.
+    auto warm = [&]() {
+      constexpr int kNodes = (1 << kWarmLevels) - 1;
+      int los[kNodes], his[kNodes];   // candidate ranges, heap order (children 2i+1, 2i+2)
+      los[0] = 0;
+      his[0] = len - 1;
+#pragma unroll
+      for (int i = 0; i < kNodes; ++i) {
+        if (los[i] < his[i]) {
+          const int mid = (los[i] + his[i] + 1) >> 1;
+          const char *row = reinterpret_cast<const char *>(kb + static_cast<size_t>(pos_of(mid)) * row_stride);
+          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row));
+          if (2 * i + 2 < kNodes) {
+            los[2 * i + 1] = los[i];
+            his[2 * i + 1] = mid - 1;
+            los[2 * i + 2] = mid;
+            his[2 * i + 2] = his[i];
+          }
+        } else if (2 * i + 2 < kNodes) {
+          los[2 * i + 1] = los[2 * i + 2] = 1;   // empty
+          his[2 * i + 1] = his[2 * i + 2] = 0;
+        }
+      }
+    };
+    if constexpr (kWarmLevels > 0) {
+      if ((sub & 3) == 0) warm();   // two lanes per row: one per 128-byte line
+    }
     // SelectRep: halve [lo, hi] at the rounded-up midpoint; the right half wins only
     // when its first token scores strictly higher than the left half's first token.
     int lo = 0, hi = len - 1;
