@@ -10,7 +10,8 @@ from dynamic_sparse_attention_gb300 import _build
 from oracle import hip
 from oracle.numerics import to_f64
 from parity import attention_errors, check_hip_row, check_hip_stage, from_dev_bits, to_dev
-from synth import decode_128k, decode_batch16, decode_case, decode_steps, decode_tiny, with_fp8_kv
+from synth import (decode_128k, decode_1m, decode_batch16, decode_case, decode_steps, decode_tiny,
+                   with_fp8_kv)
 
 pytestmark = pytest.mark.gpu
 
@@ -156,6 +157,14 @@ def test_value_shift_metamorphic():
 def test_gqa_128k_config():
     """Llama-3-8B-shaped GQA decode at context 131072 (full size, replay parity)."""
     _check_case(decode_128k())
+
+
+def test_gqa_1m_config():
+    """The bench's decode workload at full size: context 1,048,576, 32/8 heads, d=128,
+    4 pruning stages (4092 stage-0 chunks), in the launch configuration the bench times.
+    Every stage is replayed against the oracle and the attention checked in full."""
+    report = _check_case(decode_1m())
+    assert report[0][1]["band_diffs"] <= 4
 
 
 def test_batch16_config():
