@@ -3,7 +3,8 @@
 TEST INFRASTRUCTURE ONLY (see the package docstring).
 
 Source: "InfiniteHiP: Extending Language Model Context Up to 3 Million Tokens
-on a Single GPU" (paper-graph-ui summary of arXiv 2502.08910), section 3.4:
+on a Single GPU" (paper-graph-ui summary of arXiv 2502.08910), section 3.4 (and
+"Prefill Latency Details" for the chunked sparse prefill):
 "Formal Mechanism of a Single Pruning Stage" (Alg. 2 steps 1-8), "The
 Representative Token Selection Algorithm (SelectRep)" (Alg. 3), "Important:
 Sink and Streaming Tokens Are Never Pruned" (Alg. 1 line 1), "Formal
@@ -235,6 +236,60 @@ def hip_select_cached(q, K, dtype, T, chunk, keep, n_sink, n_stream, G, refresh,
         cache[i] = st.I_out
         ran[i] = st
     return ran, cache[-1]
+
+
+# ---------------------------------------------------------------- sparse prefill
+
+def prefill_block_len(S: int, m: int, b_q: int = 64) -> int:
+    """Keys a query block sees: those up to its last row, T_m = min(S, b_q (m + 1)).
+
+    Section 3.4 "Formal Mechanism of a Single Pruning Stage", step 1 (query blocks of
+    b_q = 64 rows sharing one mask); prefill is causal, so block m prunes the keys
+    before its end (the chunked prefill of "Prefill Latency Details" processes the
+    blocks 32K queries at a time over the same keys).
+    """
+    return min(S, b_q * (m + 1))
+
+
+def hip_prefill_select(q, K, dtype, S, chunk, keep, n_sink, n_stream, G, b_q: int = 64):
+    """Every query block's final selection: hip_select with the block's rows as the
+    query block and T = T_m.  q: float64 [S, H_q, D]; returns a list of index arrays."""
+    out = []
+    for m in range(math.ceil(S / b_q)):
+        rows = slice(b_q * m, min(S, b_q * (m + 1)))
+        _, I = hip_select(q[rows], K, dtype, prefill_block_len(S, m, b_q), chunk, keep,
+                          n_sink, n_stream, G)
+        out.append(I)
+    return out
+
+
+def prefill_attention(q, K, V, dtype, S, I_blocks, n_sink, n_stream, scale, G, b_q: int = 64,
+                      blocks=None):
+    """Causal attention of each query block's rows over sink + its selection + its
+    window ("Block Sparse Attention Implementation", prefill), fp64.
+
+    Row i of block m attends the keys j <= i of attended_set(T_m, n_sink, n_stream, I_m).
+    Returns {m: (O [rows, H_q, D], lse [rows, H_q])} for the blocks asked (all by default).
+    """
+    res = {}
+    H_q, D = q.shape[1], q.shape[2]
+    for m in (range(len(I_blocks)) if blocks is None else blocks):
+        r0, r1 = b_q * m, min(S, b_q * (m + 1))
+        A = attended_set(prefill_block_len(S, m, b_q), n_sink, n_stream, I_blocks[m])
+        O = np.zeros((r1 - r0, H_q, D))
+        lse = np.full((r1 - r0, H_q), -np.inf)
+        for h in range(H_q):
+            keys = to_f64(K[A, h // G], dtype)
+            vals = to_f64(V[A, h // G], dtype)
+            z = scale * (q[r0:r1, h, :] @ keys.T)
+            z[A[None, :] > np.arange(r0, r1)[:, None]] = -np.inf
+            mx = z.max(axis=1, keepdims=True)
+            p = np.exp(z - mx)
+            l = p.sum(axis=1, keepdims=True)
+            O[:, h, :] = (p @ vals) / l
+            lse[:, h] = mx[:, 0] + np.log(l[:, 0])
+        res[m] = (O, lse)
+    return res
 
 
 # ---------------------------------------------------------------- attention

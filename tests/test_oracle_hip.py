@@ -365,3 +365,53 @@ def test_e4m3_decoding_matches_torch_float8():
     # the format's landmarks: largest finite 448, smallest subnormal 2^-9, smallest normal 2^-6
     assert got[0x7E] == 448.0 and got[0x01] == 2.0 ** -9 and got[0x08] == 2.0 ** -6
     assert got[0xFE] == -448.0 and got[0x80] == 0.0
+
+
+# ------------------------------------------------------------ sparse prefill (query blocks of 64)
+
+def test_prefill_keep_all_is_dense_causal():
+    """Budgets holding every chunk: each query block attends every key before its rows,
+    so the prefill equals SDPA(is_causal)."""
+    c = decode_case("pf", B=1, T=300, T_q=300, H_q=4, H_kv=2, D=16, dtype="bf16",
+                    chunk=(16, 4), keep=(4096, 4096), n_sink=5, n_stream=7, seed=41, plant="none")
+    q64 = to_f64(c.q[0], "bf16")                                   # [S, H_q, D]
+    I = hip.hip_prefill_select(q64, c.k[0], "bf16", 300, c.chunk, c.keep, 5, 7, c.G)
+    for m, Im in enumerate(I):
+        T_m = hip.prefill_block_len(300, m)
+        assert np.array_equal(Im, hip.candidate_range(T_m, 5, 7))
+    res = hip.prefill_attention(q64, c.k[0], c.v[0], "bf16", 300, I, 5, 7, c.scale, c.G)
+    Q = torch.from_numpy(q64).permute(1, 0, 2)
+    K = torch.from_numpy(to_f64(c.k[0], "bf16")).permute(1, 0, 2).repeat_interleave(c.G, 0)
+    V = torch.from_numpy(to_f64(c.v[0], "bf16")).permute(1, 0, 2).repeat_interleave(c.G, 0)
+    ref = torch.nn.functional.scaled_dot_product_attention(Q, K, V, is_causal=True).permute(1, 0, 2)
+    for m, (O, _) in res.items():
+        np.testing.assert_allclose(O, ref[64 * m:64 * m + len(O)].numpy(), rtol=0, atol=1e-12)
+
+
+def test_prefill_block_selection_is_causal_and_keeps_sink_and_window():
+    c = decode_case("pf2", B=1, T=700, T_q=700, H_q=2, H_kv=1, D=16, dtype="bf16",
+                    chunk=(32, 8), keep=(128, 32), n_sink=8, n_stream=64, seed=42, plant="none")
+    q64 = to_f64(c.q[0], "bf16")
+    I = hip.hip_prefill_select(q64, c.k[0], "bf16", 700, c.chunk, c.keep, 8, 64, c.G)
+    for m, Im in enumerate(I):
+        T_m = hip.prefill_block_len(700, m)
+        assert np.all(Im < max(8, T_m - 64)) and np.all(Im >= 8) and len(Im) <= 32
+        A = hip.attended_set(T_m, 8, 64, Im)
+        assert np.all(np.isin(np.arange(min(8, T_m)), A))
+        assert np.all(np.isin(np.arange(max(8, T_m - 64), T_m), A))
+    # a row attends nothing after itself: the first row of block 3 and its window
+    res = hip.prefill_attention(q64, c.k[0], c.v[0], "bf16", 700, I, 8, 64, c.scale, c.G, blocks=[3])
+    O, lse = res[3]
+    assert np.isfinite(lse).all()
+
+
+def test_prefill_finds_a_planted_key_per_block():
+    """Keys 100..103 equal the mean query of block 9 (scaled up): block 9's selection
+    keeps them (chunk 8, budget 4 of the candidate chunks)."""
+    rng = np.random.default_rng(43)
+    S, D = 64 * 12, 16
+    q = rng.standard_normal((S, 1, D))
+    K = (0.3 * rng.standard_normal((S, 1, D))).astype(np.float32)
+    K[100:104, 0] = 4.0 * q[64 * 9:64 * 10, 0].mean(axis=0)
+    I = hip.hip_prefill_select(q, K, "f32", S, (8,), (32,), 4, 16, 1)
+    assert np.all(np.isin(np.arange(100, 104), I[9]))
