@@ -14,6 +14,10 @@ from .binding import (  # noqa: F401
     device_error,
     HipConfig,
     hip_max_chunks,
+    hip_prefill_lists,
+    hip_prefill_max_chunks,
+    hip_prefill_select,
+    hip_prefill_select_workspace_bytes,
     hip_select,
     hip_select_cached,
     HipSelectCache,

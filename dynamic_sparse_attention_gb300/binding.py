@@ -100,6 +100,10 @@ _SIGNATURES = {
     "mixed_index_build_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
     "mixed_index_build": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t,
                                    _vp]),
+    "dsa_hip_prefill_max_chunks": (_c_int, [_vp, _vp, _c_int, ctypes.POINTER(_c_int)]),
+    "hip_prefill_select_workspace": (_c_int, [_vp, _vp, ctypes.POINTER(ctypes.c_size_t)]),
+    "hip_prefill_select": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _vp]),
+    "hip_prefill_lists": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _vp, _vp, _vp, _vp, _vp]),
     "sparse_attn_prefill": (_c_int, [_vp, _vp, _vp, _vp, _c_int, _c_int, _c_int, _vp, _vp, _vp,
                                      _vp, ctypes.c_float, _vp, _vp, _vp]),
     "sparse_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
@@ -599,6 +603,91 @@ def mixed_index_build_workspace_bytes(q, k, *, head_pattern, last_q: int = 64,
            lib.mixed_index_build_workspace(ctypes.byref(shape), ctypes.byref(cfg), ctypes.byref(n)))
     del arr
     return n.value
+
+
+def hip_prefill_max_chunks(q, k, cfg: HipConfig, stage: int) -> int:
+    lib = load()
+    n = _c_int()
+    shape, c = prefill_shape(q, k), cfg.c()
+    _check("dsa_hip_prefill_max_chunks",
+           lib.dsa_hip_prefill_max_chunks(ctypes.byref(shape), ctypes.byref(c), stage, ctypes.byref(n)))
+    return n.value
+
+
+def hip_prefill_select_workspace_bytes(q, k, cfg: HipConfig) -> int:
+    lib = load()
+    n = ctypes.c_size_t()
+    shape, c = prefill_shape(q, k), cfg.c()
+    _check("hip_prefill_select_workspace",
+           lib.hip_prefill_select_workspace(ctypes.byref(shape), ctypes.byref(c), ctypes.byref(n)))
+    return n.value
+
+
+def hip_prefill_select(q, k, cfg: HipConfig, *, debug: bool = False, out=None, workspace=None,
+                       stream=None):
+    """InfiniteHiP pruning for every 64-row query block of a causal prefill; returns
+    (sel_idx [B * n_qblk, keep[-1]], sel_cnt [B * n_qblk][, debug dict]), rows ordered
+    b * n_qblk + m."""
+    lib = load()
+    _need_cuda(q, k)
+    shape, c = prefill_shape(q, k), cfg.c()
+    R = shape.B * ((shape.S + 63) // 64)
+    dev = q.device
+    if out is None:
+        sel_idx = torch.empty(R, cfg.keep[-1], dtype=torch.int32, device=dev)
+        sel_cnt = torch.empty(R, dtype=torch.int32, device=dev)
+    else:
+        sel_idx, sel_cnt = out
+    dbg = dbg_t = None
+    if debug:
+        dbg = HipDebug()
+        dbg_t = {"stage_idx": [], "stage_cnt": [], "chunk_score": [], "rep": [], "rep_score": []}
+        for i in range(len(cfg.chunk)):
+            mc = max(hip_prefill_max_chunks(q, k, cfg, i), 1)
+            t = {
+                "stage_idx": torch.full((R, cfg.keep[i]), -7, dtype=torch.int32, device=dev),
+                "stage_cnt": torch.full((R,), -7, dtype=torch.int32, device=dev),
+                "chunk_score": torch.full((R, mc), float("nan"), device=dev),
+                "rep": torch.full((R, shape.H_q, mc), -7, dtype=torch.int32, device=dev),
+                "rep_score": torch.full((R, shape.H_q, mc), float("nan"), device=dev),
+            }
+            for key, v in t.items():
+                dbg_t[key].append(v)
+                getattr(dbg, key)[i] = v.data_ptr()
+    ws = _workspace(hip_prefill_select_workspace_bytes(q, k, cfg), dev, workspace)
+    st = lib.hip_prefill_select(_ptr(q), _ptr(k), ctypes.byref(shape), ctypes.byref(c),
+                                _ptr(sel_idx), _ptr(sel_cnt), ctypes.byref(dbg) if dbg else None,
+                                _ptr(ws), ctypes.c_size_t(ws.numel()), _stream(stream))
+    _check("hip_prefill_select", st)
+    if debug:
+        return sel_idx, sel_cnt, dbg_t
+    return sel_idx, sel_cnt
+
+
+def hip_prefill_lists(q, k, cfg: HipConfig, sel_idx, sel_cnt, *, out: dict | None = None,
+                      stream=None):
+    """Each query block's sink + selection + window as sparse_attn_prefill lists (the
+    same for every head); returns a dict with blk_cnt, blk_idx, col_cnt, col_idx."""
+    lib = load()
+    _need_cuda(sel_idx, sel_cnt)
+    shape, c = prefill_shape(q, k), cfg.c()
+    nq = (shape.S + 63) // 64
+    max_blk = -(-cfg.n_sink // 64) + -(-cfg.n_stream // 64) + 2
+    max_col = cfg.keep[-1] + 126
+    dev = sel_idx.device
+    if out is None:
+        out = {
+            "blk_cnt": torch.empty(shape.B, shape.H_q, nq, dtype=torch.int32, device=dev),
+            "blk_idx": torch.empty(shape.B, shape.H_q, nq, max_blk, dtype=torch.int32, device=dev),
+            "col_cnt": torch.empty(shape.B, shape.H_q, nq, dtype=torch.int32, device=dev),
+            "col_idx": torch.empty(shape.B, shape.H_q, nq, max_col, dtype=torch.int32, device=dev),
+        }
+    st = lib.hip_prefill_lists(ctypes.byref(shape), ctypes.byref(c), _ptr(sel_idx), _ptr(sel_cnt),
+                               out["blk_idx"].shape[-1], out["col_idx"].shape[-1],
+                               _ptr(out["blk_cnt"]), _ptr(out["blk_idx"]), _ptr(out["col_cnt"]),
+                               _ptr(out["col_idx"]), _stream(stream))
+    _check("hip_prefill_lists", st)
+    return out
 
 
 def sparse_attn_prefill(q, k, v, blk_cnt, blk_idx, col_cnt, col_idx, *, scale=None,

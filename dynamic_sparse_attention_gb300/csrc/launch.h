@@ -170,4 +170,30 @@ cudaError_t launch_block_sparse(const BsArgs &a, cudaStream_t s);
 // query blocks per CTA of the scoring kernel (0: nb too large for shared memory)
 int bs_rows_per_cta(int nb, int D);
 
+// InfiniteHiP sparse prefill: one pruning stage's scores for query blocks of 64 rows
+// (rows r = b * n_qblk + m); the cluster of a launch spans the H_kv KV heads.
+struct PfScoreArgs {
+  const void *q, *k;            // bf16 [B, S, H_q, D], [B, S, H_kv, D]
+  int B, S, H_q, H_kv, D, n_qblk;
+  int n_sink, n_stream;
+  const int32_t *kv_rows;       // [R] keys each query block sees
+  const int32_t *in_idx, *in_cnt;   // previous stage's lists per row (NULL: stage 0)
+  int in_stride;
+  int L, max_chunks;
+  float *score;                 // [R, max_chunks]
+  int32_t *dbg_rep;             // optional [R, H_q, max_chunks]
+  float *dbg_rho;
+};
+cudaError_t launch_prefill_score(const PfScoreArgs &a, cudaStream_t s);
+cudaError_t launch_prefill_rows(int32_t *kv_rows, int R, int n_qblk, int S, cudaStream_t s);
+size_t prefill_score_smem(int D, int G, int L, bool explicit_list);
+// per-query-block selections -> prefill tile / column lists (shared by every head)
+struct PfListArgs {
+  int B, S, H_q, n_qblk, n_sink, n_stream;
+  const int32_t *sel_idx, *sel_cnt;   // [R, keep], [R]
+  int keep, max_blk, max_col;
+  int32_t *blk_cnt, *blk_idx, *col_cnt, *col_idx;   // [B, H_q, n_qblk(, max)]
+};
+cudaError_t launch_prefill_lists(const PfListArgs &a, cudaStream_t s);
+
 }  // namespace dsa

@@ -11,6 +11,8 @@
  *            block_sparse_index_build -- MInference Block-Sparse estimate (mean-pooled
  *                                   blocks, top-k_b key blocks per query block)
  *            mixed_index_build   -- one of the three patterns per head
+ *            hip_prefill_select  -- InfiniteHiP pruning per 64-row query block
+ *            hip_prefill_lists   -- its sink / selection / window as prefill lists
  *            sparse_attn_prefill -- causal attention over those 64x64 tiles and
  *                                   gathered columns
  *
@@ -288,6 +290,43 @@ int block_sparse_index_build(const void *q, const void *k, const dsa_prefill_sha
                              int block, int k_b, int max_blk, int32_t *blk_cnt, int32_t *blk_idx,
                              int32_t *col_cnt, const dsa_bs_debug *dbg, void *ws, size_t ws_bytes,
                              void *stream);
+
+/* ------------------------------------------------- InfiniteHiP sparse prefill */
+
+/* hip_prefill_select -- the pruning stages of hip_select for every query block of a
+ * causal prefill: block m (rows 64m .. 64m+63 of batch row b, one "row" r = b * n_qblk + m
+ * of the outputs, n_qblk = ceil(S/64)) prunes the keys before its end, T_m = min(S,
+ * 64 (m+1)), with the chunk score the max over every query head and every row of the
+ * block.  Source: InfiniteHiP summary, section 3.4 "Formal Mechanism of a Single
+ * Pruning Stage" (Alg. 2, b_q = 64; steps 1-7), "The Representative Token Selection
+ * Algorithm (SelectRep)", and "Prefill Latency Details" (chunked sparse prefill).
+ * q [B, S, H_q, D], k [B, S, H_kv, D] bf16; cfg as for hip_select (chunk[i] <= 256).
+ *   sel_idx [B * n_qblk, keep[n-1]] ascending key positions (-1 padded, 16-byte
+ *   aligned), sel_cnt [B * n_qblk].
+ * dbg (NULL allowed) as for hip_select with rows r in place of batch rows; its array
+ * sizes come from dsa_hip_prefill_max_chunks.  H_kv <= 8, H_q / H_kv in {1, 2, 4, 8},
+ * B * n_qblk <= 65535, D in {64, 128}; else UNSUPPORTED. */
+int hip_prefill_select_workspace(const dsa_prefill_shape *shape, const dsa_hip_cfg *cfg,
+                                 size_t *bytes);
+int dsa_hip_prefill_max_chunks(const dsa_prefill_shape *shape, const dsa_hip_cfg *cfg, int stage,
+                               int *n_chunks);
+int hip_prefill_select(const void *q, const void *k, const dsa_prefill_shape *shape,
+                       const dsa_hip_cfg *cfg, int32_t *sel_idx, int32_t *sel_cnt,
+                       const dsa_hip_debug *dbg, void *ws, size_t ws_bytes, void *stream);
+
+/* hip_prefill_lists -- each query block's attended set [0, min(n_sink, T_m)) U its
+ * selection U [max(n_sink, T_m - n_stream), T_m) as sparse_attn_prefill lists (rows
+ * attend only keys <= themselves there): the 64-key blocks wholly inside the sink or
+ * the window are tiles, every other attended key a column (ascending); every head gets
+ * the same lists.  Source: InfiniteHiP summary, "Block Sparse Attention Implementation"
+ * (prefill attention over the selected keys) and "Important: Sink and Streaming Tokens
+ * Are Never Pruned".
+ *   blk_cnt / blk_idx [B, H_q, n_qblk(, max_blk)], col_cnt / col_idx likewise with
+ *   max_col; max_blk >= ceil(n_sink/64) + ceil(n_stream/64) + 2 and
+ *   max_col >= keep[n-1] + 126, else INVALID_ARG. */
+int hip_prefill_lists(const dsa_prefill_shape *shape, const dsa_hip_cfg *cfg, const int32_t *sel_idx,
+                      const int32_t *sel_cnt, int max_blk, int max_col, int32_t *blk_cnt,
+                      int32_t *blk_idx, int32_t *col_cnt, int32_t *col_idx, void *stream);
 
 /* Mixed per-head patterns: MInference assigns each attention head one of its three
  * patterns (MInference summary, "The Three Sparse Patterns"; the assignment itself
