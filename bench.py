@@ -641,6 +641,36 @@ def main():
     patterns_line["mixed"] = dict(time_pattern(lambda: dsa.mixed_index_build(
         pq, pk, out=mix_out, workspace=ws_mix, **mix_kw), pat_steps),
         heads="h mod 3: vertical-slash, A-shape, Block-Sparse")
+    # InfiniteHiP sparse prefill on the same inputs: per-64-row query block pruning with the
+    # pages' stage table (chunks 256 / 32 / 8, keep 32768 / 8192 / 2048, sink 256,
+    # window 1024), then the prefill kernel over sink + selection + window
+    hcfg = dsa.HipConfig((256, 32, 8), (32768, 8192, 2048), 256, 1024)
+    n_rows = (pre.S + 63) // 64
+    hsel = (torch.empty(n_rows, 2048, dtype=torch.int32, device=dev),
+            torch.empty(n_rows, dtype=torch.int32, device=dev))
+    ws_h = torch.empty(dsa.hip_prefill_select_workspace_bytes(pq, pk, hcfg), dtype=torch.uint8,
+                       device=dev)
+    hl = {"blk_cnt": torch.empty(1, pre.H_q, n_rows, dtype=torch.int32, device=dev),
+          "blk_idx": torch.empty(1, pre.H_q, n_rows, 22, dtype=torch.int32, device=dev),
+          "col_cnt": torch.empty(1, pre.H_q, n_rows, dtype=torch.int32, device=dev),
+          "col_idx": torch.empty(1, pre.H_q, n_rows, 2048 + 126, dtype=torch.int32, device=dev)}
+
+    def hip_prefill_index():
+        dsa.hip_prefill_select(pq, pk, hcfg, out=hsel, workspace=ws_h)
+        dsa.hip_prefill_lists(pq, pk, hcfg, hsel[0], hsel[1], out=hl)
+        return hl
+
+    patterns_line["infinitehip"] = dict(time_pattern(hip_prefill_index, pat_steps),
+                                        chunk=[256, 32, 8], keep=[32768, 8192, 2048],
+                                        n_sink=256, n_stream=1024)
+    dsa.profile_enable(True)
+    for _ in range(pat_steps):
+        flush()
+        hip_prefill_index()
+    torch.cuda.synchronize()
+    dsa.profile_enable(False)
+    for name, (n_, t_) in dsa.profile_collect().items():
+        patterns_line["infinitehip"][f"{name}_ms"] = t_ / pat_steps
     pool_bytes = accounting.block_sparse_pool_bytes(1, pre.S, pre.H_q, pre.H_kv, pre.D)
     dsa.profile_enable(True)
     for _ in range(pat_steps):
@@ -746,7 +776,8 @@ def main():
             "attended_keys": attended,
         },
         # the same prefill kernel over MInference A-shape (1024 initial + 4096 local tokens),
-        # Block-Sparse (k_b = 100) and a per-head mix of the three patterns, same inputs
+        # Block-Sparse (k_b = 100), a per-head mix of the three patterns, and InfiniteHiP's
+        # per-query-block selection (sink + 2048 selected + 1024 window keys), same inputs
         "prefill_patterns": patterns_line,
         # the same decode step over an FP8 E4M3 copy of the KV cache (bf16 queries)
         "decode_fp8kv": fp8_line,
