@@ -152,6 +152,7 @@ int hip_prefill_select(const void *q, const void *k, const dsa_prefill_shape *sh
     sa.in_stride = i == 0 ? 0 : cfg->keep[i - 1];
     sa.L = cfg->chunk[i];
     sa.max_chunks = pf_max_chunks(shape, cfg, i);
+    sa.stage = i;
     sa.score = (dbg && dbg->chunk_score[i]) ? dbg->chunk_score[i] : w.score[i];
     sa.dbg_rep = dbg ? dbg->rep[i] : nullptr;
     sa.dbg_rho = dbg ? dbg->rep_score[i] : nullptr;

@@ -180,6 +180,7 @@ struct PfScoreArgs {
   const int32_t *in_idx, *in_cnt;   // previous stage's lists per row (NULL: stage 0)
   int in_stride;
   int L, max_chunks;
+  int stage;                    // index of the pruning stage (for timing names)
   float *score;                 // [R, max_chunks]
   int32_t *dbg_rep;             // optional [R, H_q, max_chunks]
   float *dbg_rho;

@@ -11,16 +11,18 @@
 // now a 64-row product: q_t . k for the block's 64 rows, of which the max decides.
 // That is a dense contraction, so it runs on the tensor cores (mma.sync m16n8k16,
 // bf16 in, fp32 out):
-//  * one CTA per (query block, 32 chunks, KV head g); the H_kv CTAs of a query block
+//  * one CTA per (query block, 64 chunks, KV head g); the H_kv CTAs of a query block
 //    and chunk range form a thread-block cluster;
 //  * warp w holds 16 rows of the block for query head g*G + w/4 as resident A
 //    fragments (the 64 rows of a head are four warps);
 //  * each tournament step gathers, with 16-byte cp.async, the probe row of every
-//    (head, chunk) of the CTA -- G x 32 rows of 2*D bytes for KV head g -- into an
-//    XOR-swizzled shared tile; each warp then scores its 16 rows against its head's
-//    32 probes (four n-tiles), takes the max over its rows, and the four warps of a
-//    head combine their maxima in shared memory; one thread per (head, chunk) moves
-//    the tournament on;
+//    (head, chunk) of the CTA -- G x 64 rows of 2*D bytes for KV head g -- into an
+//    XOR-swizzled shared tile (the first two steps probe the same token for every head
+//    of a chunk -- its first token, then its midpoint -- and gather one row per chunk
+//    for all of them); each warp then scores its 16 rows against its head's 64 probes
+//    (eight n-tiles), takes the max over its rows, and the four warps of a head
+//    combine their maxima in shared memory; one thread per (head, chunk) moves the
+//    tournament on;
 //  * the chunk score (max over the group's heads) of the H_kv CTAs is combined in
 //    distributed shared memory and written once.
 // Rows past the sequence end take no part (their scores are -inf).
@@ -35,7 +37,7 @@
 namespace dsa {
 namespace {
 
-constexpr int kCG = 32;    // chunks per CTA
+constexpr int kCG = 64;    // chunks per CTA
 constexpr int kBq = 64;    // query rows per block
 
 template <int D, int G>
@@ -153,8 +155,10 @@ __global__ void __launch_bounds__(G * 4 * 32) prefill_score_kernel(PfScoreArgs a
     }
     if (!__syncthreads_or(any)) break;
     // gather the probe rows (a row without a probe keeps what it held: its scores are
-    // never read)
-    for (int e = tid; e < SM::kRows * PIECES; e += NT) {
+    // never read); the first two steps probe one token per chunk for every head
+    const bool shared = step <= 1;
+    const int n_rows = shared ? kCG : SM::kRows;
+    for (int e = tid; e < n_rows * PIECES; e += NT) {
       const int i = e / PIECES, p = e - i * PIECES;
       const int x = s_x[i];
       if (x >= 0) cp16(s_k + swz<D>(i, p), kg + static_cast<size_t>(pos_of(i % kCG, x)) * kstride + p * 8);
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(G * 4 * 32) prefill_score_kernel(PfScoreArgs a
 #pragma unroll
       for (int np = 0; np < kCG / 16; ++np) {   // pairs of n-tiles: 16 probes
         float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        const int krow = hq * kCG + np * 16 + (mtx >> 1) * 8 + rr;
+        const int krow = (shared ? 0 : hq * kCG) + np * 16 + (mtx >> 1) * 8 + rr;
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           uint32_t bk[4];
@@ -347,7 +351,9 @@ cudaError_t launch_prefill_rows(int32_t *kv_rows, int R, int n_qblk, int S, cuda
 cudaError_t launch_prefill_score(const PfScoreArgs &a, cudaStream_t s) {
   if (a.max_chunks == 0) return cudaSuccess;
   const int G = a.H_q / a.H_kv;
-  ProfScope ps("prefill_stage_score", s);
+  static const char *const kNames[4] = {"prefill_stage_score_s0", "prefill_stage_score_s1",
+                                        "prefill_stage_score_s2", "prefill_stage_score_s3+"};
+  ProfScope ps(kNames[a.stage < 3 ? a.stage : 3], s);
   if (a.D == 128) {
     switch (G) {
       case 1: return launch_pf<128, 1>(a, s);

@@ -9,6 +9,8 @@ Workloads (seeded generators of the `synth` module at the repository root):
   prefill_128k vs_index_build + sparse_attn_prefill, S=131072, 32/8 heads, d=128
   prefill_16k  the same at S=16384
   prefill_bs_32k  block_sparse_index_build (k_b=100) + sparse_attn_prefill at S=32768
+  prefill_hip_16k  hip_prefill_select + hip_prefill_lists + sparse_attn_prefill at S=16384
+                   (chunks 256 / 32 / 8, keep 4096 / 2048 / 1024, sink 256, window 1024)
 Each iteration launches the workload's kernels once on the current stream; nothing is
 timed or checked.  The first iteration is a warm-up like any other, so a profiler
 that skips the first launches of a kernel sees steady-state ones.
@@ -63,10 +65,23 @@ def _prefill_bs(case, iters, k_b=100):
     torch.cuda.synchronize()
 
 
+def _prefill_hip(case, iters, cfg):
+    import torch
+
+    from . import binding as dsa
+    q, k, v = _to_dev(case.q, torch), _to_dev(case.k, torch), _to_dev(case.v, torch)
+    for _ in range(iters):
+        sel, cnt = dsa.hip_prefill_select(q, k, cfg)
+        lists = dsa.hip_prefill_lists(q, k, cfg, sel, cnt)
+        dsa.sparse_attn_prefill(q, k, v, lists["blk_cnt"], lists["blk_idx"], lists["col_cnt"],
+                                lists["col_idx"])
+    torch.cuda.synchronize()
+
+
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("workload", choices=["decode_1m", "decode_128k", "prefill_128k", "prefill_16k",
-                                        "prefill_bs_32k"])
+                                        "prefill_bs_32k", "prefill_hip_16k"])
     p.add_argument("--iters", type=int, default=4)
     args = p.parse_args(argv)
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -80,6 +95,9 @@ def main(argv=None):
         _decode(synth.decode_128k(), args.iters)
     elif args.workload == "prefill_128k":
         _prefill(synth.prefill_128k(), args.iters)
+    elif args.workload == "prefill_hip_16k":
+        _prefill_hip(synth.prefill_case("prefill_hip_S16384", S=16384, H_q=32, H_kv=8, D=128, seed=4),
+                     args.iters, dsa.HipConfig((256, 32, 8), (4096, 2048, 1024), 256, 1024))
     elif args.workload == "prefill_bs_32k":
         _prefill_bs(synth.prefill_case("prefill_bs_S32768", S=32768, H_q=32, H_kv=8, D=128, seed=4),
                     args.iters)
