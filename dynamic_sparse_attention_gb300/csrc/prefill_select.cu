@@ -60,8 +60,9 @@ __device__ __forceinline__ int swz(int row, int piece) {   // element offset, 8 
   return row * D + ((piece ^ (row & 7)) << 3);
 }
 
+// two CTAs per SM (up to G = 4): the tournaments of both are in flight at once
 template <int D, int G>
-__global__ void __launch_bounds__(G * 4 * 32) prefill_score_kernel(PfScoreArgs a) {
+__global__ void __launch_bounds__(G * 4 * 32, G <= 4 ? 2 : 1) prefill_score_kernel(PfScoreArgs a) {
   namespace cg = cooperative_groups;
   using SM = PfSmem<D, G>;
   constexpr int NT = G * 4 * 32;
@@ -311,6 +312,9 @@ cudaError_t launch_pf(const PfScoreArgs &a, cudaStream_t s) {
   const size_t smem = PfSmem<D, G>::bytes(a.L, a.in_idx != nullptr);
   auto kern = prefill_score_kernel<D, G>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  // all of the unified L1 / shared memory as shared memory, so two CTAs fit an SM
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   if (e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((a.max_chunks + kCG - 1) / kCG, a.H_kv, a.B * a.n_qblk);
