@@ -34,6 +34,10 @@ sys.path.insert(0, ROOT)
 
 METRIC = "sparse-attn decode μs/step @1M ctx; prefill ms @128K; % HBM / TC roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# the nominal denominators the targets are stated against: about 8 TB/s of HBM3e and the
+# dense bf16 tensor-core peak of a GB300 (2.25 PFLOP/s)
+NOMINAL_HBM_GBS = 8000.0
+NOMINAL_BF16_TFLOPS = 2250.0
 # DRAM bytes read + written per launch, from ncu captures of the kernels as they are
 # now (profiles/hip_stage_score_s0_decode_1m.md, profiles/prefill_attention_tc_S131072.md);
 # keyed by (kernel, workload).  Remove an entry when its kernel changes.
@@ -563,6 +567,8 @@ def main():
                 "frac": achieved / hbm if achieved else None,
                 "traffic": NCU_TRAFFIC.get((dom, dec.name)),
                 "peak_source": f"{peaks_src} hbm_gbs",
+                "nominal_peak": NOMINAL_HBM_GBS,
+                "frac_nominal": achieved / NOMINAL_HBM_GBS if achieved else None,
                 "algorithmic_bytes_per_launch": dom_bytes}
 
     # prefill tiles and FLOPs
@@ -583,6 +589,8 @@ def main():
                         "unit": "TFLOP/s", "frac": tflops / tc_peak,
                         "traffic": NCU_TRAFFIC.get((att_name, pre.name)),
                         "peak_source": f"{peaks_src} bf16_tflops_sustained (kernel timed inside a long step)",
+                        "nominal_peak": NOMINAL_BF16_TFLOPS,
+                        "frac_nominal": tflops / NOMINAL_BF16_TFLOPS,
                         "algorithmic_flops_per_launch": flops}
 
     # ---------------- other MInference head patterns on the same prefill kernel
