@@ -575,6 +575,8 @@ def main():
     blk_cnt = idx["blk_cnt"].cpu().numpy()
     col_cnt = idx["col_cnt"].cpu().numpy()
     flops = accounting.prefill_tile_flops(blk_cnt, col_cnt, pre.D)
+    useful_flops = accounting.prefill_useful_flops(blk_cnt, idx["blk_idx"].cpu().numpy(), col_cnt,
+                                                   idx["col_idx"].cpu().numpy(), pre.S, pre.D)
     tiles = int(blk_cnt.sum() + np.ceil(col_cnt / 64.0).sum())
     dense_tiles = accounting.causal_dense_tiles(pre.S) * pre.H_q
     att_name = [n for n in kern if n.startswith("prefill_attention")][0]
@@ -800,6 +802,10 @@ def main():
             "tile_density_vs_causal_dense": tiles / dense_tiles,
             "tile_flops": flops,
             "vs_index_GBps": vs_bytes / (vs_us * 1e-6) / 1e9,
+            "vs_index_hbm_frac": vs_bytes / (vs_us * 1e-6) / 1e9 / hbm,
+            # pairs (query row, key) the lists make attended, causal masking subtracted
+            "useful_flops": useful_flops,
+            "useful_TFLOPs": useful_flops / (att_us * 1e-6) / 1e12,
         },
         # the step's dominant kernel (prefill attention, >99% of a step's GPU time)
         "roofline": roofline_prefill,

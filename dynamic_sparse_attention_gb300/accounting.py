@@ -71,6 +71,32 @@ def prefill_tile_flops(blk_cnt: np.ndarray, col_cnt: np.ndarray, D: int) -> floa
     return float(tiles) * 4.0 * 64 * 64 * D
 
 
+def prefill_useful_flops(blk_cnt, blk_idx, col_cnt, col_idx, S: int, D: int) -> float:
+    """4 * D flops per (query row, key) pair the lists make a row attend: a listed block
+    before the row's own block counts 64 x 64 pairs, the diagonal block the causal
+    triangle, a listed column j of query block m the rows of m at or after j; rows and
+    keys past the sequence end count nothing.  Lists are [B, H, n_qblk(, max)] arrays."""
+    nq = blk_cnt.shape[-1]
+    m = np.arange(nq)[None, None, :]
+    rows = np.minimum(64, S - 64 * m)                                 # rows of block m
+    width = blk_idx.shape[-1]
+    valid_b = np.arange(width)[None, None, None, :] < blk_cnt[..., None]
+    n = np.where(valid_b, blk_idx, -1)
+    key_w = np.clip(S - 64 * n, 0, 64)                                 # keys in block n
+    below = (n >= 0) & (n < m[..., None])
+    diag = (n == m[..., None])
+    tri = rows * (rows + 1) // 2                                       # diagonal triangle
+    pairs = (np.where(below, rows[..., None] * key_w, 0).sum() +
+             np.where(diag, tri[..., None], 0).sum())
+    cw = col_idx.shape[-1]
+    if cw:
+        valid_c = np.arange(cw)[None, None, None, :] < col_cnt[..., None]
+        j = np.where(valid_c, col_idx, S)
+        last = 64 * m[..., None] + rows[..., None]                     # one past the last row
+        pairs += np.where(valid_c, np.clip(last - np.maximum(j, 64 * m[..., None]), 0, None), 0).sum()
+    return float(pairs) * 4.0 * D
+
+
 def vs_index_bytes(B, S, H_q, H_kv, D, n_vertical, elem=2) -> float:
     """Two passes over K (row statistics, then sums) + the estimate rows of Q."""
     return float(2 * B * S * H_kv * D * elem + 2 * B * 64 * H_q * D * elem)

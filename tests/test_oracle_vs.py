@@ -157,3 +157,30 @@ def test_page_cost_formulas(golden):
     assert abs(g["last_q"] * g["S"] * g["d"] - g["flops"]) <= g["rel_tol"] * g["flops"]
     b = golden["block_sparse_speedup_1m"]
     assert abs(b["S"] / (2 * b["B"] * b["k_b"]) - b["speedup_approx"]) <= b["rel_tol"] * 78
+
+
+def test_useful_flop_count_matches_the_tile_mask():
+    """The bench's count of attended (row, key) pairs equals the dense mask's count."""
+    from dynamic_sparse_attention_gb300 import accounting
+    for S in (300, 256, 97):
+        rng = np.random.default_rng(S)
+        nq = (S + 63) // 64
+        blk, col = [], []
+        for m in range(nq):
+            b = np.sort(rng.choice(m + 1, size=int(rng.integers(0, m + 2)), replace=False))
+            covered = np.zeros(S, bool)
+            for n in b:
+                covered[64 * n:min(S, 64 * n + 64)] = True
+            cand = np.nonzero(~covered[:min(S, 64 * m + 64)])[0]
+            c = np.sort(rng.choice(cand, size=min(5, len(cand)), replace=False)) if len(cand) else np.zeros(0, int)
+            blk.append(b)
+            col.append(c)
+        M = vs.tile_mask(blk, col, S)
+        bc = np.array([[[len(b) for b in blk]]])
+        cc = np.array([[[len(c) for c in col]]])
+        bi = np.full((1, 1, nq, nq), -1)
+        ci = np.full((1, 1, nq, 5), -1)
+        for m in range(nq):
+            bi[0, 0, m, :len(blk[m])] = blk[m]
+            ci[0, 0, m, :len(col[m])] = col[m]
+        assert accounting.prefill_useful_flops(bc, bi, cc, ci, S, 1) == 4.0 * M.sum()
