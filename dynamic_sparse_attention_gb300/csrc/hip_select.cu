@@ -15,10 +15,13 @@
 // is already known; each iteration therefore loads exactly one new key row.
 #include <math.h>
 
+#include <algorithm>
+
 #include <type_traits>
 
 #include "common.cuh"
 #include "launch.h"
+#include "mma_sync.cuh"
 
 namespace dsa {
 namespace {
@@ -47,12 +50,29 @@ __device__ __forceinline__ InputRange stage_input(const int32_t *kv_len, int b, 
   return r;
 }
 
-// smem layout shared with the host-side size computation below
-__host__ __device__ inline size_t score_smem_pos_off() { return 128 * sizeof(float); }
-__host__ __device__ inline size_t score_smem_q_off(bool explicit_list, int L) {
-  size_t o = score_smem_pos_off() + (explicit_list ? ((static_cast<size_t>(L) + 3) & ~size_t(3)) * 4 : 0);
-  return o;
-}
+// Chunks of at most this many tokens are scored from shared memory: the CTA copies all
+// key rows of its chunks in one round (every KV head of a token is one contiguous run)
+// and the tournaments read them there, instead of a chain of dependent row loads.  Such
+// a CTA takes up to kMaxChunksPerCta chunks, so that a stage of many small chunks runs
+// in about one wave.
+constexpr int kSmemRowsMaxL = 4;
+constexpr int kMaxChunksPerCta = 4;
+constexpr int kRhoMax = 512;   // per-CTA head maxima: chunks per CTA x H_q
+
+// shared-memory layout, the same on both sides: head maxima, positions, fp32 query
+// rows (multi-row blocks), staged key rows
+struct ScoreSmem {
+  size_t pos, q, rows, total;
+  __host__ __device__ ScoreSmem(bool rows_mode, bool explicit_list, int L, int C, bool qreg, int T_q,
+                                int H_q, int D, size_t row_bytes) {
+    pos = kRhoMax * sizeof(float);
+    const size_t npos = rows_mode ? static_cast<size_t>(C) * L : (explicit_list ? L : 0);
+    q = pos + ((npos + 3) & ~size_t(3)) * sizeof(int);
+    size_t o = q + (qreg ? 0 : static_cast<size_t>(T_q) * H_q * D * sizeof(float));
+    rows = (o + 15) & ~size_t(15);
+    total = rows + (rows_mode ? static_cast<size_t>(C) * L * row_bytes : 0);
+  }
+};
 
 // tournament levels whose candidate rows are requested from L2 ahead of time
 constexpr int kWarmLevels = 2;
@@ -62,25 +82,63 @@ constexpr int kWarmLevels = 2;
 // a time, so the number of tournaments in flight is what feeds HBM.
 // TQ / TK: storage of the query (bf16 or fp32) and of the key rows (the same, or FP8
 // E4M3 under a bf16 query).
-template <typename TQ, typename TK, int D, bool QREG, int NT_MAX, int MIN_B>
-__global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreArgs a) {
+// ROWS: the key rows of the CTA's C chunks (C * L <= kMaxChunksPerCta * kSmemRowsMaxL
+// tokens) are staged in shared memory; otherwise C = 1 and the rows are read as the
+// tournament needs them.
+template <typename TQ, typename TK, int D, bool QREG, int NT_MAX, int MIN_B, bool ROWS>
+__global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreArgs a, int C) {
   constexpr int EPL = D / 8;
+  if (!ROWS) C = 1;
+  const size_t row_stride = static_cast<size_t>(a.H_kv) * D;   // elements per token
   extern __shared__ __align__(16) unsigned char smem[];
   float *s_rho = reinterpret_cast<float *>(smem);
-  int *s_pos = reinterpret_cast<int *>(smem + score_smem_pos_off());
-  float *s_q = reinterpret_cast<float *>(smem + score_smem_q_off(a.in_idx != nullptr, a.L));
+  int *s_pos, *s_q_raw;
+  uint4 *s_rows;
+  {
+    const ScoreSmem lay(ROWS, a.in_idx != nullptr, a.L, C, QREG, a.T_q, a.H_q, D, row_stride * sizeof(TK));
+    s_pos = reinterpret_cast<int *>(smem + lay.pos);
+    s_q_raw = reinterpret_cast<int *>(smem + lay.q);
+    s_rows = reinterpret_cast<uint4 *>(smem + lay.rows);
+  }
+  float *s_q = reinterpret_cast<float *>(s_q_raw);
 
   grid_dep_wait();
-  const int b = blockIdx.y, j = blockIdx.x;
+  const int b = blockIdx.y, j0 = blockIdx.x * C;
+  const TK *kbase = static_cast<const TK *>(a.k) + static_cast<size_t>(b) * a.T_max * row_stride;
+  const int32_t *lst = a.in_idx ? a.in_idx + static_cast<size_t>(b) * a.in_stride : nullptr;
+  // The list entries are read before the list's count, which only bounds what is used
+  // below: a read stays inside the row of the list, and a position (possibly stale) is
+  // clamped to the key rows.
+  int pv = 0;
+  if (ROWS) {
+    // all heads of the C * L tokens, 16-byte asynchronous copies (all in flight at once)
+    const int per_tok = static_cast<int>(row_stride * sizeof(TK) / 16);
+    const int n_u = C * a.L * per_tok;
+#pragma unroll 4
+    for (int u = threadIdx.x; u < n_u; u += blockDim.x) {
+      const int x = u / per_tok, w = u - x * per_tok;
+      const int p = j0 * a.L + x;
+      const int pos = lst ? min(max(__ldg(lst + min(p, a.in_stride - 1)), 0), a.T_max - 1)
+                          : min(a.n_sink + p, a.T_max - 1);
+      if (w == 0) s_pos[x] = pos;
+      cp_async_16(s_rows + u, reinterpret_cast<const uint4 *>(kbase + static_cast<size_t>(pos) * row_stride) + w);
+    }
+    cp_async_commit();
+  } else if (lst && static_cast<int>(threadIdx.x) < a.L) {
+    pv = __ldg(lst + min(j0 * a.L + static_cast<int>(threadIdx.x), a.in_stride - 1));
+  }
   const InputRange ir = stage_input(a.kv_len, b, a.T_max, a.n_sink, a.n_stream, a.in_idx,
                                     a.in_cnt, a.in_stride);
   const int n_chunk = (ir.n_in + a.L - 1) / a.L;
-  if (j >= n_chunk) return;
-  const int base = j * a.L;
-  const int len = min(a.L, ir.n_in - base);
+  if (j0 >= n_chunk) {
+    if (ROWS) cp_async_wait<0>();   // no copy outlives the CTA
+    return;
+  }
   const TQ *q = static_cast<const TQ *>(a.q) + static_cast<size_t>(b) * a.T_q * a.H_q * D;
-  if (ir.in) {   // a cached list may be stale: never read outside the key rows
-    for (int x = threadIdx.x; x < len; x += blockDim.x) s_pos[x] = min(max(ir.in[base + x], 0), a.T_max - 1);
+  if (!ROWS && ir.in) {
+    const int len0 = min(a.L, ir.n_in - j0 * a.L);
+    for (int x = threadIdx.x; x < len0; x += blockDim.x)
+      s_pos[x] = min(max(x == static_cast<int>(threadIdx.x) ? pv : ir.in[j0 * a.L + x], 0), a.T_max - 1);
   }
   if (!QREG) {
     const int n = a.T_q * a.H_q * D;
@@ -89,10 +147,12 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
       else s_q[e] = reinterpret_cast<const float *>(q)[e];
     }
   }
+  if (ROWS) cp_async_wait<0>();
   __syncthreads();
 
   const int h = threadIdx.x >> 3, sub = threadIdx.x & 7;
   const int G = a.H_q / a.H_kv;
+  const int n_here = min(C, n_chunk - j0);   // chunks of this CTA that exist
   if (h < a.H_q) {
     const int g = h / G;
     const unsigned omask = 0xffu << (threadIdx.x & 24);
@@ -106,124 +166,139 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
 #pragma unroll
       for (int i = 0; i < NVQ; ++i) qraw[i] = __ldg(qp + i);
     }
-    const TK *kb = static_cast<const TK *>(a.k) + static_cast<size_t>(b) * a.T_max * a.H_kv * D +
-                   static_cast<size_t>(g) * D + sub * EPL;
-    const size_t row_stride = static_cast<size_t>(a.H_kv) * D;
+    const TK *kb = kbase + static_cast<size_t>(g) * D + sub * EPL;
     const int T_q = QREG ? 1 : a.T_q;
-    auto pos_of = [&](int x) -> int { return ir.in ? s_pos[x] : ir.start + base + x; };
-    auto score = [&](int x) -> float {
-      // keep the row as raw 16-byte words and widen while multiplying (fewer registers)
-      uint4 raw[NV];
-      const uint4 *kp = reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(pos_of(x)) * row_stride);
+    for (int c = 0; c < n_here; ++c) {
+      const int j = j0 + c;
+      const int base = j * a.L;
+      const int len = min(a.L, ir.n_in - base);
+      // position of the chunk's x-th token
+      auto pos_of = [&](int x) -> int {
+        return ROWS ? s_pos[c * a.L + x] : (ir.in ? s_pos[x] : ir.start + base + x);
+      };
+      auto score = [&](int x) -> float {
+        // keep the row as raw 16-byte words and widen while multiplying (fewer registers)
+        uint4 raw[NV];
+        if (ROWS) {
+          const uint4 *kp = s_rows + (static_cast<size_t>(c * a.L + x) * row_stride +
+                                      static_cast<size_t>(g) * D + sub * EPL) * sizeof(TK) / 16;
 #pragma unroll
-      for (int i = 0; i < NV; ++i) raw[i] = __ldg(kp + i);
-      float best = -INFINITY;
-      for (int t = 0; t < T_q; ++t) {
-        const float *qq = s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
-        float d = 0.f;
-        if constexpr (std::is_same<TQ, TK>::value) {
-          constexpr int per = Store<TK>::kPer16;
-#pragma unroll
-          for (int i = 0; i < NV; ++i) {
-            float kf[per], qf[per];
-            unpack16(raw[i], kf, TK());
-            if (QREG) unpack16(qraw[i], qf, TQ());
-#pragma unroll
-            for (int e = 0; e < per; ++e) d = fmaf(QREG ? qf[e] : qq[i * per + e], kf[e], d);
-          }
+          for (int i = 0; i < NV; ++i) raw[i] = kp[i];
         } else {
-          // FP8 keys under a bf16 query: each 32-bit key word is four elements, matched by
-          // two 32-bit query words
+          const uint4 *kp = reinterpret_cast<const uint4 *>(kb + static_cast<size_t>(pos_of(x)) * row_stride);
 #pragma unroll
-          for (int i = 0; i < NV; ++i) {
-            const uint32_t kw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+          for (int i = 0; i < NV; ++i) raw[i] = __ldg(kp + i);
+        }
+        float best = -INFINITY;
+        for (int t = 0; t < T_q; ++t) {
+          const float *qq = s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
+          float d = 0.f;
+          if constexpr (std::is_same<TQ, TK>::value) {
+            constexpr int per = Store<TK>::kPer16;
 #pragma unroll
-            for (int wi = 0; wi < 4; ++wi) {
-              const int e0 = 16 * i + 4 * wi;   // first element of this word in the slice
+            for (int i = 0; i < NV; ++i) {
+              float kf[per], qf[per];
+              unpack16(raw[i], kf, TK());
+              if (QREG) unpack16(qraw[i], qf, TQ());
 #pragma unroll
-              for (int bb = 0; bb < 4; ++bb) {
-                const float kf = e4m3_to_f32((kw[wi] >> (8 * bb)) & 0xFFu);
-                float qf;
-                if (QREG) {
-                  const uint4 &qv = qraw[(e0 + bb) >> 3];
-                  const int qw = ((e0 + bb) >> 1) & 3;
-                  const uint32_t word = qw == 0 ? qv.x : qw == 1 ? qv.y : qw == 2 ? qv.z : qv.w;
-                  qf = ((e0 + bb) & 1) ? bf16_hi(word) : bf16_lo(word);
-                } else {
-                  qf = qq[e0 + bb];
+              for (int e = 0; e < per; ++e) d = fmaf(QREG ? qf[e] : qq[i * per + e], kf[e], d);
+            }
+          } else {
+            // FP8 keys under a bf16 query: each 32-bit key word is four elements, matched
+            // by two 32-bit query words
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+              const uint32_t kw[4] = {raw[i].x, raw[i].y, raw[i].z, raw[i].w};
+#pragma unroll
+              for (int wi = 0; wi < 4; ++wi) {
+                const int e0 = 16 * i + 4 * wi;   // first element of this word in the slice
+#pragma unroll
+                for (int bb = 0; bb < 4; ++bb) {
+                  const float kf = e4m3_to_f32((kw[wi] >> (8 * bb)) & 0xFFu);
+                  float qf;
+                  if (QREG) {
+                    const uint4 &qv = qraw[(e0 + bb) >> 3];
+                    const int qw = ((e0 + bb) >> 1) & 3;
+                    const uint32_t word = qw == 0 ? qv.x : qw == 1 ? qv.y : qw == 2 ? qv.z : qv.w;
+                    qf = ((e0 + bb) & 1) ? bf16_hi(word) : bf16_lo(word);
+                  } else {
+                    qf = qq[e0 + bb];
+                  }
+                  d = fmaf(qf, kf, d);
                 }
-                d = fmaf(qf, kf, d);
               }
             }
           }
+          d += __shfl_xor_sync(omask, d, 4);
+          d += __shfl_xor_sync(omask, d, 2);
+          d += __shfl_xor_sync(omask, d, 1);
+          best = fmaxf(best, d);
         }
-        d += __shfl_xor_sync(omask, d, 4);
-        d += __shfl_xor_sync(omask, d, 2);
-        d += __shfl_xor_sync(omask, d, 1);
-        best = fmaxf(best, d);
-      }
-      return best;
-    };
-    // The first kWarmLevels probes of every head's tournament can only be one of the
-    // 2^level - 1 midpoints of the first levels (the same for every head of the chunk):
-    // ask L2 for those rows now, in the round of the first load, so those levels' loads
-    // hit L2 instead of each waiting a DRAM round.
-    auto warm = [&]() {
-      constexpr int kNodes = (1 << kWarmLevels) - 1;
-      int los[kNodes], his[kNodes];   // candidate ranges, heap order (children 2i+1, 2i+2)
-      los[0] = 0;
-      his[0] = len - 1;
+        return best;
+      };
+      // The first kWarmLevels probes of every head's tournament can only be one of the
+      // 2^level - 1 midpoints of the first levels (the same for every head of the
+      // chunk): ask L2 for those rows now, in the round of the first load, so those
+      // levels' loads hit L2 instead of each waiting a DRAM round.
+      auto warm = [&]() {
+        constexpr int kNodes = (1 << kWarmLevels) - 1;
+        int los[kNodes], his[kNodes];   // candidate ranges, heap order (children 2i+1, 2i+2)
+        los[0] = 0;
+        his[0] = len - 1;
 #pragma unroll
-      for (int i = 0; i < kNodes; ++i) {
-        if (los[i] < his[i]) {
-          const int mid = (los[i] + his[i] + 1) >> 1;
-          const char *row = reinterpret_cast<const char *>(kb + static_cast<size_t>(pos_of(mid)) * row_stride);
-          asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row));
-          if (2 * i + 2 < kNodes) {
-            los[2 * i + 1] = los[i];
-            his[2 * i + 1] = mid - 1;
-            los[2 * i + 2] = mid;
-            his[2 * i + 2] = his[i];
+        for (int i = 0; i < kNodes; ++i) {
+          if (los[i] < his[i]) {
+            const int mid = (los[i] + his[i] + 1) >> 1;
+            const char *row = reinterpret_cast<const char *>(kb + static_cast<size_t>(pos_of(mid)) * row_stride);
+            asm volatile("prefetch.global.L2 [%0];\n" ::"l"(row));
+            if (2 * i + 2 < kNodes) {
+              los[2 * i + 1] = los[i];
+              his[2 * i + 1] = mid - 1;
+              los[2 * i + 2] = mid;
+              his[2 * i + 2] = his[i];
+            }
+          } else if (2 * i + 2 < kNodes) {
+            los[2 * i + 1] = los[2 * i + 2] = 1;   // empty
+            his[2 * i + 1] = his[2 * i + 2] = 0;
           }
-        } else if (2 * i + 2 < kNodes) {
-          los[2 * i + 1] = los[2 * i + 2] = 1;   // empty
-          his[2 * i + 1] = his[2 * i + 2] = 0;
+        }
+      };
+      if constexpr (kWarmLevels > 0 && !ROWS) {
+        if ((sub & 3) == 0) warm();   // two lanes per row: one per 128-byte line
+      }
+      // SelectRep: halve [lo, hi] at the rounded-up midpoint; the right half wins only
+      // when its first token scores strictly higher than the left half's first token.
+      int lo = 0, hi = len - 1;
+      float s_lo = score(0);
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const float s_mid = score(mid);
+        if (s_mid > s_lo) {
+          lo = mid;
+          s_lo = s_mid;
+        } else {
+          hi = mid - 1;
         }
       }
-    };
-    if constexpr (kWarmLevels > 0) {
-      if ((sub & 3) == 0) warm();   // two lanes per row: one per 128-byte line
-    }
-    // SelectRep: halve [lo, hi] at the rounded-up midpoint; the right half wins only
-    // when its first token scores strictly higher than the left half's first token.
-    int lo = 0, hi = len - 1;
-    float s_lo = score(0);
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      const float s_mid = score(mid);
-      if (s_mid > s_lo) {
-        lo = mid;
-        s_lo = s_mid;
-      } else {
-        hi = mid - 1;
-      }
-    }
-    if (sub == 0) {
-      s_rho[h] = s_lo;
-      if (a.dbg_rep) {
-        const size_t o = (static_cast<size_t>(b) * a.H_q + h) * a.max_chunks + j;
-        a.dbg_rep[o] = pos_of(lo);
-        if (a.dbg_rho) a.dbg_rho[o] = s_lo;
+      if (sub == 0) {
+        s_rho[c * a.H_q + h] = s_lo;
+        if (a.dbg_rep) {
+          const size_t o = (static_cast<size_t>(b) * a.H_q + h) * a.max_chunks + j;
+          a.dbg_rep[o] = pos_of(lo);
+          if (a.dbg_rho) a.dbg_rho[o] = s_lo;
+        }
       }
     }
   }
   __syncthreads();
-  // chunk score: max over all query heads (and rows, already inside s_rho)
-  if (threadIdx.x < 32) {
+  // chunk score: max over all query heads (and rows, already inside s_rho), one warp
+  // per chunk
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  for (int c = warp; c < n_here; c += blockDim.x >> 5) {
     float m = -INFINITY;
-    for (int i = threadIdx.x; i < a.H_q; i += 32) m = fmaxf(m, s_rho[i]);
+    for (int i = lane; i < a.H_q; i += 32) m = fmaxf(m, s_rho[c * a.H_q + i]);
     m = warp_max(m);
-    if (threadIdx.x == 0) a.score[static_cast<size_t>(b) * a.max_chunks + j] = m;
+    if (lane == 0) a.score[static_cast<size_t>(b) * a.max_chunks + j0 + c] = m;
   }
 }
 
@@ -301,9 +376,14 @@ constexpr int kFastNT = 1024;
 constexpr int kFastNPT = 16;
 constexpr int kFastNB = 4096;
 constexpr int kFastCand = 1024;
+constexpr int kTopkMaxParts = 8;         // CTAs writing one row's list
+constexpr int kTopkPartEntries = 2048;   // list entries per part, at least
 
-// inclusive block scan of one value per thread (thread order); all threads call it
+// inclusive block scan of one value per thread (thread order); all threads call it.
+// One barrier: every warp reads all warp totals and forms its own offset.  Two scans in
+// a row must use different s_w buffers (a slow warp may still read the first).
 __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *s_w, uint32_t *total) {
+  static_assert(kFastNT == 1024, "one warp total per lane");
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   uint32_t incl = v;
 #pragma unroll
@@ -313,22 +393,9 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t v, uint32_t *s_w, u
   }
   if (lane == 31) s_w[warp] = incl;
   __syncthreads();
-  if (warp == 0) {
-    const uint32_t x = lane < kFastNT / 32 ? s_w[lane] : 0u;
-    uint32_t w = x;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const uint32_t u = __shfl_up_sync(kFull, w, o);
-      if (lane >= o) w += u;
-    }
-    if (lane < kFastNT / 32) s_w[lane] = w - x;
-    if (lane == 31) s_w[kFastNT / 32] = w;
-  }
-  __syncthreads();
-  const uint32_t r = s_w[warp] + incl;
-  *total = s_w[kFastNT / 32];
-  __syncthreads();   // s_w may be reused right away
-  return r;
+  const uint32_t x = s_w[lane];
+  *total = __reduce_add_sync(kFull, x);
+  return __reduce_add_sync(kFull, lane < warp ? x : 0u) + incl;
 }
 
 // POW2: 16-byte access to the score row and the token lists (see the host side).
@@ -342,7 +409,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
   __shared__ uint32_t s_ckey[kFastCand];
   __shared__ int s_cidx[kFastCand];
   __shared__ uint32_t s_keep[(NT * NPT + 31) / 32];   // kept bits of boundary-bucket chunks
-  __shared__ uint32_t s_w[NT / 32 + 1];
+  __shared__ uint32_t s_w[3][NT / 32];   // one buffer per block scan
   __shared__ uint32_t s_misc[8];   // 0 min, 1 max, 2 boundary bucket, 3 count above, 4 candidates
   __shared__ uint32_t s_hist8[256];
   __shared__ uint32_t s_res[2];
@@ -399,17 +466,10 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
     }
     if (tid == 0) s_misc[4] = 0u;
     __syncthreads();
-    if (warp == 0) {
-      const uint32_t m0 = __reduce_min_sync(kFull, s_hist8[lane]);
-      const uint32_t m1 = __reduce_max_sync(kFull, s_hist8[32 + lane]);
-      if (lane == 0) {
-        s_misc[0] = m0;
-        s_misc[1] = m1;
-      }
-    }
-    __syncthreads();
-    const uint32_t kmin = s_misc[0];
-    const float bscale = static_cast<float>(NB) / (static_cast<float>(s_misc[1] - kmin) + 1.0f);
+    // every warp reduces the 32 warp partials itself (no second barrier)
+    const uint32_t kmin = __reduce_min_sync(kFull, s_hist8[lane]);
+    const uint32_t kmax = __reduce_max_sync(kFull, s_hist8[32 + lane]);
+    const float bscale = static_cast<float>(NB) / (static_cast<float>(kmax - kmin) + 1.0f);
     // never decreasing in the key: a uint32 -> float conversion keeps order (ties at
     // worst), as do the positive scaling and the truncation
     auto bucket = [&](uint32_t u) {
@@ -427,7 +487,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
       sum4 += c4[j];
     }
     uint32_t total;
-    const uint32_t incl = block_incl_scan(sum4, s_w, &total);
+    const uint32_t incl = block_incl_scan(sum4, s_w[0], &total);
     const uint32_t K = static_cast<uint32_t>(a.K);
     if (incl - sum4 < K && K <= incl) {
       uint32_t run = incl - sum4;
@@ -543,7 +603,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
 #pragma unroll
       for (int k = 0; k < NPT; ++k) eq += (i0 + k < n_chunk && key[k] == thr) ? 1u : 0u;
       uint32_t tot_eq;
-      uint32_t eq_b = block_incl_scan(eq, s_w, &tot_eq) - eq;
+      uint32_t eq_b = block_incl_scan(eq, s_w[1], &tot_eq) - eq;
       kept_bits = 0u;
 #pragma unroll
       for (int k = 0; k < NPT; ++k) {
@@ -560,7 +620,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
   // ranks of the kept chunks in index order
   const uint32_t nk = static_cast<uint32_t>(__popc(kept_bits));
   uint32_t tot_kept;
-  uint32_t r = block_incl_scan(nk, s_w, &tot_kept) - nk;
+  uint32_t r = block_incl_scan(nk, s_w[2], &tot_kept) - nk;
 #pragma unroll
   for (int k = 0; k < NPT; ++k) {
     if ((kept_bits >> k) & 1u) {
@@ -575,28 +635,45 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
   if (n_kept > 0 && s_chunk_of_rank[n_kept - 1] == n_chunk - 1) count -= n_chunk * L - ir.n_in;
   int32_t *out = a.out_idx + static_cast<size_t>(b) * a.out_stride;
   int32_t *dbg = a.dbg_idx ? a.dbg_idx + static_cast<size_t>(b) * a.out_stride : nullptr;
+  // this CTA's part of the list (every part repeats the selection above)
+  const int part_len = (((a.out_stride + gridDim.y - 1) / gridDim.y) + 3) & ~3;
+  const int e_beg = min(a.out_stride, static_cast<int>(blockIdx.y) * part_len);
+  const int e_end = min(a.out_stride, e_beg + part_len);
   if (POW2 && (L & 3) == 0 && (a.out_stride & 3) == 0) {
-    // four consecutive entries share a chunk: 16-byte loads and stores
+    // four consecutive entries share a chunk: 16-byte loads and stores, kU gathers in
+    // flight per thread before their stores
+    constexpr int kU = 4;
     const int lg = __ffs(L) - 1;
-    for (int e = 4 * tid; e < a.out_stride; e += 4 * NT) {
-      int4 val = make_int4(-1, -1, -1, -1);
-      if (e < count) {
-        const int rr = e >> lg, x = e & (L - 1);
-        const int src = (s_chunk_of_rank[rr] << lg) + x;
-        if (ir.in) {
-          val = *reinterpret_cast<const int4 *>(ir.in + src);
-        } else {
-          val = make_int4(ir.start + src, ir.start + src + 1, ir.start + src + 2, ir.start + src + 3);
+    for (int e0 = e_beg + 4 * tid; e0 < e_end; e0 += 4 * NT * kU) {
+      int4 val[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + 4 * NT * u;
+        val[u] = make_int4(-1, -1, -1, -1);
+        if (e < count) {
+          const int rr = e >> lg, x = e & (L - 1);
+          const int src = (s_chunk_of_rank[rr] << lg) + x;
+          if (ir.in) {
+            val[u] = *reinterpret_cast<const int4 *>(ir.in + src);
+          } else {
+            val[u] = make_int4(ir.start + src, ir.start + src + 1, ir.start + src + 2, ir.start + src + 3);
+          }
+          if (e + 1 >= count) val[u].y = -1;
+          if (e + 2 >= count) val[u].z = -1;
+          if (e + 3 >= count) val[u].w = -1;
         }
-        if (e + 1 >= count) val.y = -1;
-        if (e + 2 >= count) val.z = -1;
-        if (e + 3 >= count) val.w = -1;
       }
-      *reinterpret_cast<int4 *>(out + e) = val;
-      if (dbg) *reinterpret_cast<int4 *>(dbg + e) = val;
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int e = e0 + 4 * NT * u;
+        if (e < e_end) {
+          *reinterpret_cast<int4 *>(out + e) = val[u];
+          if (dbg) *reinterpret_cast<int4 *>(dbg + e) = val[u];
+        }
+      }
     }
   } else {
-    for (int e = tid; e < a.out_stride; e += NT) {
+    for (int e = e_beg + tid; e < e_end; e += NT) {
       int val = -1;
       if (e < count) {
         const int rr = e / L, x = e - rr * L;
@@ -607,7 +684,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
       if (dbg) dbg[e] = val;
     }
   }
-  if (tid == 0) {
+  if (tid == 0 && blockIdx.y == 0) {
     a.out_cnt[b] = count;
     if (a.dbg_cnt) a.dbg_cnt[b] = count;
   }
@@ -617,20 +694,57 @@ template <typename TQ, typename TK, int D>
 cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
   const bool explicit_list = a.in_idx != nullptr;
   const bool qreg = a.T_q == 1;
-  size_t smem = score_smem_q_off(explicit_list, a.L);
-  if (!qreg) smem += static_cast<size_t>(a.T_q) * a.H_q * D * sizeof(float);
   const int threads = ((8 * a.H_q + 31) / 32) * 32;
-  dim3 grid(a.max_chunks, a.B);
   if (a.max_chunks == 0) return cudaSuccess;
+  // fp32 rows need twice the registers: six CTAs per SM there; the staged-rows variant
+  // loops over its chunks and keeps two CTAs fewer
+  constexpr int kMinB = sizeof(TQ) == 2 ? 8 : 6;
+  constexpr int kMinBRows = kMinB - 2;
+  const size_t row_bytes = static_cast<size_t>(a.H_kv) * D * sizeof(TK);
+  constexpr size_t kRowsSmemMax = 64 * 1024;   // staged rows per CTA
+  constexpr size_t kSmemPerSm = 228 * 1024;     // 1 KB of it reserved per CTA
+  const bool rows = a.L <= kSmemRowsMaxL && (!qreg || threads <= 256) && a.L * row_bytes <= kRowsSmemMax;
+  int C = 1;
+  if (rows) {
+    // The fewest chunks per CTA that hold the whole stage in one wave of resident CTAs
+    // (registers and shared memory both bound the CTAs per SM); failing that, the most
+    // chunks in flight.
+    static const int n_sm = [] {
+      int dev = 0, n = 0;
+      cudaGetDevice(&dev);
+      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+      return n > 0 ? n : 1;
+    }();
+    const long long need = static_cast<long long>(a.B) * a.max_chunks;
+    long long best = -1;
+    for (int c = 1; c <= kMaxChunksPerCta; ++c) {
+      if (c * a.H_q > kRhoMax || c * a.L * row_bytes > kRowsSmemMax) break;
+      const size_t bytes = ScoreSmem(true, explicit_list, a.L, c, qreg, a.T_q, a.H_q, D, row_bytes).total;
+      const long long per_sm = std::min<long long>(qreg ? kMinBRows : 1, (kSmemPerSm / (bytes + 1024)));
+      const long long cap = static_cast<long long>(n_sm) * per_sm * c;
+      if (cap > best) {
+        best = cap;
+        C = c;
+      }
+      if (cap >= need) break;
+    }
+  }
+  const ScoreSmem lay(rows, explicit_list, a.L, C, qreg, a.T_q, a.H_q, D, row_bytes);
+  const size_t smem = lay.total;
+  dim3 grid((a.max_chunks + C - 1) / C, a.B);
   auto go = [&](auto kern) {
     if (smem > 48 * 1024) cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch_pdl(kern, grid, dim3(threads), smem, s, a);
+    launch_pdl(kern, grid, dim3(threads), smem, s, a, C);
   };
-  // fp32 rows need twice the registers: six CTAs per SM there
-  constexpr int kMinB = sizeof(TQ) == 2 ? 8 : 6;
-  if (qreg && threads <= 256) go(stage_score_kernel<TQ, TK, D, true, 256, kMinB>);
-  else if (qreg) go(stage_score_kernel<TQ, TK, D, true, 1024, 1>);
-  else go(stage_score_kernel<TQ, TK, D, false, 1024, 1>);
+  if (qreg && threads <= 256) {
+    if (rows) go(stage_score_kernel<TQ, TK, D, true, 256, kMinBRows, true>);
+    else go(stage_score_kernel<TQ, TK, D, true, 256, kMinB, false>);
+  } else if (qreg) {
+    go(stage_score_kernel<TQ, TK, D, true, 1024, 1, false>);
+  } else {
+    if (rows) go(stage_score_kernel<TQ, TK, D, false, 1024, 1, true>);
+    else go(stage_score_kernel<TQ, TK, D, false, 1024, 1, false>);
+  }
   return cudaGetLastError();
 }
 
@@ -648,10 +762,14 @@ cudaError_t launch_stage_score(const StageScoreArgs &a, cudaStream_t s) {
 cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s) {
   const size_t smem = static_cast<size_t>(a.K) * sizeof(int);
   // static shared memory: about 28 KB in the register-resident kernel, 1 KB otherwise
-  auto go = [&](auto kern, int threads, size_t static_bytes) {
+  // The register-resident kernel spreads the list writes over `parts` CTAs per row,
+  // each repeating the (cheap, deterministic) selection: one SM alone writes a list of
+  // tens of thousands of entries at a fraction of the L2 bandwidth.
+  const int parts = std::max(1, std::min(kTopkMaxParts, (a.out_stride + kTopkPartEntries - 1) / kTopkPartEntries));
+  auto go = [&](auto kern, int threads, size_t static_bytes, int nparts) {
     if (smem + static_bytes > 48 * 1024)
       cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    launch_pdl(kern, dim3(a.B), dim3(threads), smem, s, a);
+    launch_pdl(kern, dim3(a.B, nparts), dim3(threads), smem, s, a);
   };
   // 16-byte list access needs 16-byte aligned rows of the explicit input list, and rows
   // holding whole chunks (the last chunk's 16-byte groups then stay inside the row)
@@ -665,16 +783,16 @@ cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s) {
   if (a.max_chunks <= kFastNT * kFastNPT) {
     auto pick = [&](auto pw) {
       constexpr bool P = decltype(pw)::value;
-      if (a.max_chunks <= kFastNT) go(stage_topk_fast_kernel<P, 1>, kFastNT, 28 * 1024);
-      else if (a.max_chunks <= 2 * kFastNT) go(stage_topk_fast_kernel<P, 2>, kFastNT, 28 * 1024);
-      else if (a.max_chunks <= 4 * kFastNT) go(stage_topk_fast_kernel<P, 4>, kFastNT, 28 * 1024);
-      else if (a.max_chunks <= 8 * kFastNT) go(stage_topk_fast_kernel<P, 8>, kFastNT, 28 * 1024);
-      else go(stage_topk_fast_kernel<P, 16>, kFastNT, 28 * 1024);
+      if (a.max_chunks <= kFastNT) go(stage_topk_fast_kernel<P, 1>, kFastNT, 28 * 1024, parts);
+      else if (a.max_chunks <= 2 * kFastNT) go(stage_topk_fast_kernel<P, 2>, kFastNT, 28 * 1024, parts);
+      else if (a.max_chunks <= 4 * kFastNT) go(stage_topk_fast_kernel<P, 4>, kFastNT, 28 * 1024, parts);
+      else if (a.max_chunks <= 8 * kFastNT) go(stage_topk_fast_kernel<P, 8>, kFastNT, 28 * 1024, parts);
+      else go(stage_topk_fast_kernel<P, 16>, kFastNT, 28 * 1024, parts);
     };
     if (pow2) pick(std::true_type{});
     else pick(std::false_type{});
   } else {
-    go(stage_topk_kernel, kTopkThreads, 2 * 1024);
+    go(stage_topk_kernel, kTopkThreads, 2 * 1024, 1);
   }
   return cudaGetLastError();
 }
