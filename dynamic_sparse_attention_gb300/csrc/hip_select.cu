@@ -74,7 +74,8 @@ struct ScoreSmem {
   }
 };
 
-// tournament levels whose candidate rows are requested from L2 ahead of time
+// tournament levels whose candidate rows are requested from L2 ahead of time (a third
+// level, four candidates of which a head probes one, measured slower)
 constexpr int kWarmLevels = 2;
 
 // NT_MAX / MIN_B: launch bounds.  Up to 32 query heads (256 threads) the kernel keeps
@@ -496,6 +497,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
         if (run + c4[j] >= K) {
           s_misc[2] = static_cast<uint32_t>(NB - 1 - 4 * tid - j);
           s_misc[3] = run;
+          s_misc[5] = c4[j];
           break;
         }
         run += c4[j];
@@ -504,114 +506,121 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
     __syncthreads();
     const int bstar = static_cast<int>(s_misc[2]);
     const uint32_t above = s_misc[3];
-    // the boundary bucket's members
+    if (s_misc[5] == K - above) {
+      // the whole boundary bucket is in the top K (the usual case: one key there)
 #pragma unroll
-    for (int k = 0; k < NPT; ++k) {
-      const bool valid = i0 + k < n_chunk;
-      const int bk = valid ? bucket(key[k]) : -1;
-      if (bk > bstar) kept_bits |= 1u << k;
-      // one slot claim per warp and key position
-      const unsigned members = __ballot_sync(kFull, bk == bstar);
-      if (members) {
-        uint32_t base = 0;
-        if (lane == __ffs(members) - 1) base = atomicAdd(&s_misc[4], static_cast<uint32_t>(__popc(members)));
-        base = __shfl_sync(kFull, base, __ffs(members) - 1);
-        if (bk == bstar) {
-          const uint32_t slot = base + __popc(members & ((1u << lane) - 1u));
-          if (slot < static_cast<uint32_t>(kFastCand)) {
-            s_ckey[slot] = key[k];
-            s_cidx[slot] = i0 + k;
-          }
-        }
-      }
-    }
-    __syncthreads();
-    const uint32_t m = s_misc[4];
-    if (m <= static_cast<uint32_t>(kFastCand)) {
-      // exact ranks inside the bucket: larger key first, then smaller chunk index
-      const uint32_t need = K - above;   // 1 <= need <= m
-      for (uint32_t j = tid; j < m; j += NT) {
-        const uint32_t kj = s_ckey[j];
-        const int ij = s_cidx[j];
-        uint32_t rank = 0;
-        for (uint32_t i = 0; i < m; ++i) {
-          const uint32_t ki = s_ckey[i];
-          rank += (ki > kj || (ki == kj && s_cidx[i] < ij)) ? 1u : 0u;
-        }
-        if (rank < need) atomicOr(&s_keep[ij >> 5], 1u << (ij & 31));
-      }
-      __syncthreads();
+      for (int k = 0; k < NPT; ++k)
+        if (i0 + k < n_chunk && bucket(key[k]) >= bstar) kept_bits |= 1u << k;
+    } else {
+      // the boundary bucket's members
 #pragma unroll
       for (int k = 0; k < NPT; ++k) {
-        const int i = i0 + k;
-        if (i < n_chunk && bucket(key[k]) == bstar && ((s_keep[i >> 5] >> (i & 31)) & 1u))
-          kept_bits |= 1u << k;
-      }
-    } else {
-      // many equal or nearly equal keys: radix select over the resident keys for the
-      // K-th largest key `thr` and the number `k_eq` of its copies in the top K, then
-      // keep the first k_eq copies in index order
-      uint32_t prefix = 0u, mask = 0u, k_rem = K;
-      for (int pass = 0; pass < 4; ++pass) {
-        const int shift = 24 - 8 * pass;
-        for (int i = tid; i < 256; i += NT) s_hist8[i] = 0u;
-        __syncthreads();
-#pragma unroll
-        for (int k = 0; k < NPT; ++k) {
-          const bool ok = i0 + k < n_chunk && (key[k] & mask) == prefix;
-          const uint32_t bin = ok ? ((key[k] >> shift) & 255u) : 256u;
-          const unsigned peers = __match_any_sync(kFull, bin);
-          if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist8[bin], static_cast<uint32_t>(__popc(peers)));
-        }
-        __syncthreads();
-        if (warp == 0) {
-          const int top = 255 - lane * 8;
-          uint32_t c[8], sum = 0;
-#pragma unroll
-          for (int t = 0; t < 8; ++t) {
-            c[t] = s_hist8[top - t];
-            sum += c[t];
-          }
-          uint32_t inc = sum;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t v = __shfl_up_sync(kFull, inc, o);
-            if (lane >= o) inc += v;
-          }
-          const uint32_t exc = inc - sum;
-          if (exc < k_rem && k_rem <= inc) {
-            uint32_t run = exc;
-#pragma unroll
-            for (int t = 0; t < 8; ++t) {
-              if (run + c[t] >= k_rem) {
-                s_res[0] = static_cast<uint32_t>(top - t);
-                s_res[1] = run;
-                break;
-              }
-              run += c[t];
+        const bool valid = i0 + k < n_chunk;
+        const int bk = valid ? bucket(key[k]) : -1;
+        if (bk > bstar) kept_bits |= 1u << k;
+        // one slot claim per warp and key position
+        const unsigned members = __ballot_sync(kFull, bk == bstar);
+        if (members) {
+          uint32_t base = 0;
+          if (lane == __ffs(members) - 1) base = atomicAdd(&s_misc[4], static_cast<uint32_t>(__popc(members)));
+          base = __shfl_sync(kFull, base, __ffs(members) - 1);
+          if (bk == bstar) {
+            const uint32_t slot = base + __popc(members & ((1u << lane) - 1u));
+            if (slot < static_cast<uint32_t>(kFastCand)) {
+              s_ckey[slot] = key[k];
+              s_cidx[slot] = i0 + k;
             }
           }
         }
-        __syncthreads();
-        prefix |= s_res[0] << shift;
-        mask |= 255u << shift;
-        k_rem -= s_res[1];
-        __syncthreads();
       }
-      const uint32_t thr = prefix, k_eq = k_rem;
-      uint32_t eq = 0;
+      __syncthreads();
+      const uint32_t m = s_misc[4];
+      if (m <= static_cast<uint32_t>(kFastCand)) {
+        // exact ranks inside the bucket: larger key first, then smaller chunk index
+        const uint32_t need = K - above;   // 1 <= need <= m
+        for (uint32_t j = tid; j < m; j += NT) {
+          const uint32_t kj = s_ckey[j];
+          const int ij = s_cidx[j];
+          uint32_t rank = 0;
+          for (uint32_t i = 0; i < m; ++i) {
+            const uint32_t ki = s_ckey[i];
+            rank += (ki > kj || (ki == kj && s_cidx[i] < ij)) ? 1u : 0u;
+          }
+          if (rank < need) atomicOr(&s_keep[ij >> 5], 1u << (ij & 31));
+        }
+        __syncthreads();
 #pragma unroll
-      for (int k = 0; k < NPT; ++k) eq += (i0 + k < n_chunk && key[k] == thr) ? 1u : 0u;
-      uint32_t tot_eq;
-      uint32_t eq_b = block_incl_scan(eq, s_w[1], &tot_eq) - eq;
-      kept_bits = 0u;
+        for (int k = 0; k < NPT; ++k) {
+          const int i = i0 + k;
+          if (i < n_chunk && bucket(key[k]) == bstar && ((s_keep[i >> 5] >> (i & 31)) & 1u))
+            kept_bits |= 1u << k;
+        }
+      } else {
+        // many equal or nearly equal keys: radix select over the resident keys for the
+        // K-th largest key `thr` and the number `k_eq` of its copies in the top K, then
+        // keep the first k_eq copies in index order
+        uint32_t prefix = 0u, mask = 0u, k_rem = K;
+        for (int pass = 0; pass < 4; ++pass) {
+          const int shift = 24 - 8 * pass;
+          for (int i = tid; i < 256; i += NT) s_hist8[i] = 0u;
+          __syncthreads();
 #pragma unroll
-      for (int k = 0; k < NPT; ++k) {
-        if (i0 + k < n_chunk) {
-          if (key[k] > thr) kept_bits |= 1u << k;
-          if (key[k] == thr) {
-            if (eq_b < k_eq) kept_bits |= 1u << k;
-            ++eq_b;
+          for (int k = 0; k < NPT; ++k) {
+            const bool ok = i0 + k < n_chunk && (key[k] & mask) == prefix;
+            const uint32_t bin = ok ? ((key[k] >> shift) & 255u) : 256u;
+            const unsigned peers = __match_any_sync(kFull, bin);
+            if (ok && lane == __ffs(peers) - 1) atomicAdd(&s_hist8[bin], static_cast<uint32_t>(__popc(peers)));
+          }
+          __syncthreads();
+          if (warp == 0) {
+            const int top = 255 - lane * 8;
+            uint32_t c[8], sum = 0;
+#pragma unroll
+            for (int t = 0; t < 8; ++t) {
+              c[t] = s_hist8[top - t];
+              sum += c[t];
+            }
+            uint32_t inc = sum;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+              const uint32_t v = __shfl_up_sync(kFull, inc, o);
+              if (lane >= o) inc += v;
+            }
+            const uint32_t exc = inc - sum;
+            if (exc < k_rem && k_rem <= inc) {
+              uint32_t run = exc;
+#pragma unroll
+              for (int t = 0; t < 8; ++t) {
+                if (run + c[t] >= k_rem) {
+                  s_res[0] = static_cast<uint32_t>(top - t);
+                  s_res[1] = run;
+                  break;
+                }
+                run += c[t];
+              }
+            }
+          }
+          __syncthreads();
+          prefix |= s_res[0] << shift;
+          mask |= 255u << shift;
+          k_rem -= s_res[1];
+          __syncthreads();
+        }
+        const uint32_t thr = prefix, k_eq = k_rem;
+        uint32_t eq = 0;
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) eq += (i0 + k < n_chunk && key[k] == thr) ? 1u : 0u;
+        uint32_t tot_eq;
+        uint32_t eq_b = block_incl_scan(eq, s_w[1], &tot_eq) - eq;
+        kept_bits = 0u;
+#pragma unroll
+        for (int k = 0; k < NPT; ++k) {
+          if (i0 + k < n_chunk) {
+            if (key[k] > thr) kept_bits |= 1u << k;
+            if (key[k] == thr) {
+              if (eq_b < k_eq) kept_bits |= 1u << k;
+              ++eq_b;
+            }
           }
         }
       }
