@@ -12,7 +12,13 @@
 // contiguous 16-byte loads and the dot product closes with three xor-shuffles (the
 // same value lands in all eight lanes, so every lane takes the same branch).  The
 // tournament's left representative is always the current range start, whose score
-// is already known; each iteration therefore loads exactly one new key row.
+// is already known; each iteration therefore loads exactly one new key row.  Chunks of
+// at most four tokens are scored from shared memory instead: one CTA copies all key
+// rows of a few chunks in one round and runs their tournaments there.
+//
+// Layout of the top-K kernel: the row's chunk scores in registers, a bucket select for
+// the K-th score, a block scan for the ranks of the kept chunks; the token list is
+// written by several CTAs of the row, each repeating the selection.
 #include <math.h>
 
 #include <algorithm>
