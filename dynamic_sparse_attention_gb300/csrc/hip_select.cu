@@ -724,12 +724,10 @@ cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
     // The fewest chunks per CTA that hold the whole stage in one wave of resident CTAs
     // (registers and shared memory both bound the CTAs per SM); failing that, the most
     // chunks in flight.
-    static const int n_sm = [] {
-      int dev = 0, n = 0;
-      cudaGetDevice(&dev);
-      cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-      return n > 0 ? n : 1;
-    }();
+    int dev = 0, n_sm = 0;   // the current device's (a process may drive several)
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n_sm, cudaDevAttrMultiProcessorCount, dev);
+    n_sm = std::max(n_sm, 1);
     const long long need = static_cast<long long>(a.B) * a.max_chunks;
     long long best = -1;
     for (int c = 1; c <= kMaxChunksPerCta; ++c) {
