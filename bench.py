@@ -237,6 +237,18 @@ def cpu_baseline(dec, pre):
     }
 
 
+def max_over_ranks(values, world, device):
+    """The per-rank times reduced to their maximum over all ranks (every rank gets it);
+    one rank returns them unchanged.  The replicas exchange nothing else."""
+    if world <= 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x) for x in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def run_reference(args, rank):
     """The oracle as it stands on the host cores (rank 0 only)."""
     if rank != 0:
@@ -740,10 +752,7 @@ def main():
     # ---------------- max over ranks
     dec_us = 1e3 * statistics.mean(dec_ms)
     pre_ms = statistics.mean(idx_ms) + statistics.mean(att_ms)
-    if world > 1:
-        t = torch.tensor([dec_us, pre_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dec_us, pre_ms = float(t[0]), float(t[1])
+    dec_us, pre_ms = max_over_ranks([dec_us, pre_ms], world, dev)
     if rank != 0:
         dist.destroy_process_group()
         return
