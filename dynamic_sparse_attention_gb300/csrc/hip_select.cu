@@ -219,9 +219,14 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
 #pragma unroll
               for (int wi = 0; wi < 4; ++wi) {
                 const int e0 = 16 * i + 4 * wi;   // first element of this word in the slice
+                // the word's four codes widened by the hardware conversion (E4M3 -> f16 ->
+                // f32, both exact: the same values as a bit-level decode)
+                float k4[4];
+                f16x2_to_f32x2(e4m3x2_to_f16x2(kw[wi]), k4[0], k4[1]);
+                f16x2_to_f32x2(e4m3x2_to_f16x2(kw[wi] >> 16), k4[2], k4[3]);
 #pragma unroll
                 for (int bb = 0; bb < 4; ++bb) {
-                  const float kf = e4m3_to_f32((kw[wi] >> (8 * bb)) & 0xFFu);
+                  const float kf = k4[bb];
                   float qf;
                   if (QREG) {
                     const uint4 &qv = qraw[(e0 + bb) >> 3];

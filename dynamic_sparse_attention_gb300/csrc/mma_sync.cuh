@@ -44,6 +44,13 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   return r;
 }
 
+// the two halves of an f16x2 word as floats (exact), low half first
+__device__ __forceinline__ void f16x2_to_f32x2(uint32_t h2, float &lo, float &hi) {
+  asm("{\n.reg .f16 l, h;\nmov.b32 {l, h}, %2;\ncvt.f32.f16 %0, l;\ncvt.f32.f16 %1, h;\n}\n"
+      : "=f"(lo), "=f"(hi)
+      : "r"(h2));
+}
+
 __device__ __forceinline__ unsigned smem_addr(const void *p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
 }
