@@ -200,7 +200,18 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
         for (int t = 0; t < T_q; ++t) {
           const float *qq = s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
           float d = 0.f;
-          if constexpr (std::is_same<TQ, TK>::value) {
+          if constexpr (std::is_same<TQ, TK>::value && sizeof(TK) == 2 && QREG) {
+            // bf16 query and key words straight into a mixed-precision FMA (bf16 inputs
+            // widened exactly, fp32 accumulate): the same products and order as widening
+            // first, without the widening instructions
+#pragma unroll
+            for (int i = 0; i < NV; ++i) {
+              d = fma_bf16x2_acc(qraw[i].x, raw[i].x, d);
+              d = fma_bf16x2_acc(qraw[i].y, raw[i].y, d);
+              d = fma_bf16x2_acc(qraw[i].z, raw[i].z, d);
+              d = fma_bf16x2_acc(qraw[i].w, raw[i].w, d);
+            }
+          } else if constexpr (std::is_same<TQ, TK>::value) {
             constexpr int per = Store<TK>::kPer16;
 #pragma unroll
             for (int i = 0; i < NV; ++i) {

@@ -44,6 +44,16 @@ __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t x) {
   return r;
 }
 
+// d + q.lo * k.lo, then + q.hi * k.hi, for two bf16x2 words: each step one fp32 FMA of
+// the exactly widened bf16 inputs (one rounding), low halves first
+__device__ __forceinline__ float fma_bf16x2_acc(uint32_t q, uint32_t k, float d) {
+  asm("{\n.reg .b16 ql, qh, kl, kh;\nmov.b32 {ql, qh}, %1;\nmov.b32 {kl, kh}, %2;\n"
+      "fma.rn.f32.bf16 %0, ql, kl, %0;\nfma.rn.f32.bf16 %0, qh, kh, %0;\n}\n"
+      : "+f"(d)
+      : "r"(q), "r"(k));
+  return d;
+}
+
 // the two halves of an f16x2 word as floats (exact), low half first
 __device__ __forceinline__ void f16x2_to_f32x2(uint32_t h2, float &lo, float &hi) {
   asm("{\n.reg .f16 l, h;\nmov.b32 {l, h}, %2;\ncvt.f32.f16 %0, l;\ncvt.f32.f16 %1, h;\n}\n"
