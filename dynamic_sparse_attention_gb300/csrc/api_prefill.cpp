@@ -2,8 +2,6 @@
 // block_sparse_index_build and sparse_attn_prefill.
 #include <algorithm>
 #include <cmath>
-#include <cstdlib>
-#include <cstring>
 
 #include "api_common.h"
 #include "launch.h"
@@ -297,7 +295,9 @@ int sparse_attn_prefill(const void *q, const void *k, const void *v,
   if (st) return st;
   if (block != kBlock) return fail(DSA_ERR_UNSUPPORTED, "block=%d (only 64)", block);
   if (max_blk < 0 || max_col < 0) return fail(DSA_ERR_INVALID_ARG, "max_blk / max_col negative");
-  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "scale is not finite");
+  // the kernel orders scores by their raw value, which needs a positive scale
+  if (!std::isfinite(scale) || !(scale > 0.f))
+    return fail(DSA_ERR_INVALID_ARG, "scale=%g must be positive and finite", scale);
   if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
     return fail(DSA_ERR_ALIGNMENT, "q, k, v and out must be non-NULL and 16-byte aligned");
   if (!aligned(blk_cnt, 4) || !aligned(col_cnt, 4) || (max_blk > 0 && !aligned(blk_idx, 4)) ||
@@ -322,12 +322,8 @@ int sparse_attn_prefill(const void *q, const void *k, const void *v,
   a.scale = scale;
   a.out = out;
   a.lse = lse;
-  // tcgen05 kernel by default; DSA_PREFILL_IMPL=mma selects the warp-MMA kernel (used to
-  // compare the two on the same inputs)
-  const char *impl = std::getenv("DSA_PREFILL_IMPL");
-  const bool use_mma = (impl && std::strcmp(impl, "mma") == 0) || !prefill_tc_supported(a);
-  cudaError_t e = use_mma ? launch_prefill_mma(a, static_cast<cudaStream_t>(stream))
-                          : launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
+  if ((st = prefill_tc_check(a))) return st;
+  cudaError_t e = launch_prefill_tc(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "sparse_attn_prefill launch");
   return DSA_OK;
 }

@@ -81,6 +81,12 @@ struct DecodeArgs {
   float *lse;
 };
 cudaError_t launch_decode(const DecodeArgs &a, cudaStream_t s);
+// Host validation of a decode call and its arguments, everything but `part`
+// (api_decode.cpp); *part_floats = the split-K partials the plan needs (0: none).
+int decode_prepare(const void *q, const void *k, const void *v, const int32_t *kv_len,
+                   const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, int n_sink,
+                   int n_stream, float scale, const dsa_decode_shape *shape, void *out,
+                   float *lse, DecodeArgs *args, size_t *part_floats);
 
 // Decode plan shared by the workspace query and the launch.
 //  * cluster path (cluster = true): one thread-block cluster of n_split CTAs per
@@ -140,9 +146,10 @@ struct PrefillArgs {
   void *out;
   float *lse;
 };
-cudaError_t launch_prefill_mma(const PrefillArgs &a, cudaStream_t s);
-// tcgen05 version (D in {64, 128}; shared-memory budget bounds S)
-bool prefill_tc_supported(const PrefillArgs &a);
+// The tcgen05 kernel's own limits (D in {64, 128}, positive scale, the bitmaps of one
+// query-block pair in shared memory, the driver's tensor-map encoder): DSA_OK, or a
+// status with the reason in dsa_last_error().
+int prefill_tc_check(const PrefillArgs &a);
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s);
 
 // MInference A-shape block lists (static: the initial blocks plus a band ending at the

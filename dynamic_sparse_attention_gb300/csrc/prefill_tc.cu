@@ -725,14 +725,19 @@ cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
 }  // namespace
 
 // The kernel orders scores by their raw value, which needs a positive scale; it also
-// needs D in {64, 128} and the bitmaps of one query-block pair in shared memory.
-bool prefill_tc_supported(const PrefillArgs &a) {
-  if (a.D != 64 && a.D != 128) return false;
-  if (!(a.scale > 0.f)) return false;
+// needs D in {64, 128}, the bitmaps of one query-block pair in shared memory and the
+// driver's tensor-map encoder.
+int prefill_tc_check(const PrefillArgs &a) {
+  if (a.D != 64 && a.D != 128) return fail(DSA_ERR_UNSUPPORTED, "D=%d not in {64, 128}", a.D);
+  if (!(a.scale > 0.f)) return fail(DSA_ERR_INVALID_ARG, "scale=%g must be positive", a.scale);
   const int n_qblk = (a.S + kBlk - 1) / kBlk;
   const size_t smem = a.D == 128 ? Layout<128>::bytes((n_qblk + 31) / 32)
                                  : Layout<64>::bytes((n_qblk + 31) / 32);
-  return smem <= 227 * 1024 && encode_fn() != nullptr;
+  if (smem > 227 * 1024)
+    return fail(DSA_ERR_UNSUPPORTED, "S=%d: %zu bytes of shared memory per CTA > 227 KiB", a.S, smem);
+  if (encode_fn() == nullptr)
+    return fail(DSA_ERR_UNSUPPORTED, "the driver offers no cuTensorMapEncodeTiled entry point");
+  return DSA_OK;
 }
 
 cudaError_t launch_prefill_tc(const PrefillArgs &a, cudaStream_t s) {

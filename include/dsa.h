@@ -188,8 +188,10 @@ int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_
  * argument.  A call whose scratch (sparse_attn_decode_workspace) exceeds
  * 4 MiB is rejected with DSA_ERR_WORKSPACE and launches nothing.
  * The first call on a device looks up the array's device address (device
- * current at the call) and caches it; make that first call before any stream
- * capture.  All calls share the one array and nothing in it needs clearing
+ * current at the call) and caches it for that device's current context; make
+ * that first call before any stream capture.  After a cudaDeviceReset the
+ * first call in the new context looks the address up again (the same rule:
+ * not inside a capture).  All calls share the one array and nothing in it needs clearing
  * (each call overwrites the slots it reads), but calls that overlap on the
  * GPU (other streams, other threads) race on it: serialise them. */
 int sparse_attn_decode_noalloc(const void *q, const void *k, const void *v,
@@ -374,7 +376,10 @@ int mixed_index_build(const void *q, const void *k, const dsa_prefill_shape *sha
  *   col_idx [B, H_q, n_qblk, max_col]  key positions < S, distinct, not inside a
  *                                      listed block (else counted twice)
  * out [B, S, H_q, D] bf16; lse [B, H_q, S] fp32 natural log (NULL to skip).
- * A row with no attended key gets out = 0, lse = -inf.  block must be 64. */
+ * A row with no attended key gets out = 0, lse = -inf.  block must be 64; scale
+ * must be positive and finite (INVALID_ARG otherwise: the kernel orders scores by
+ * their raw value).  S is bounded by the shared memory that holds the tile bitmaps
+ * of one query-block pair (UNSUPPORTED beyond it). */
 int sparse_attn_prefill(const void *q, const void *k, const void *v,
                         const dsa_prefill_shape *shape, int block, int max_blk, int max_col,
                         const int32_t *blk_cnt, const int32_t *blk_idx, const int32_t *col_cnt,

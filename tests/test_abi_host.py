@@ -216,3 +216,16 @@ def test_fp8_kv_shapes(lib):
     assert b"FP8" in lib.dsa_last_error()
     s = _shape(dtype=3)
     assert lib.hip_select_workspace(ctypes.byref(s), ctypes.byref(c), ctypes.byref(n)) == -2
+
+
+def test_prefill_rejects_a_non_positive_scale(lib):
+    """The prefill kernel orders scores by their raw value: scale <= 0 is an argument
+    error, rejected before any launch (there is no second kernel to fall back to)."""
+    s = _pshape()
+    buf = (ctypes.c_char * 64)()
+    ok = ctypes.c_void_p(ctypes.addressof(buf) + (-ctypes.addressof(buf) % 16))
+    for bad in (0.0, -1.0, float("inf")):
+        st = lib.sparse_attn_prefill(ok, ok, ok, ctypes.byref(s), 64, 4, 4, ok, ok, ok, ok,
+                                     ctypes.c_float(bad), ok, None, None)
+        assert st == -1
+        assert b"scale" in lib.dsa_last_error()
