@@ -97,6 +97,62 @@ long attended_max(const dsa_decode_shape *s, int max_sel, int n_sink, int n_stre
 }
 
 }  // namespace
+
+// Validation and argument fill-in shared by sparse_attn_decode and
+// sparse_attn_decode_noalloc; everything but the partials pointer.  *part_floats is the
+// split-K scratch the plan needs (0 on the cluster path).
+int decode_prepare(const void *q, const void *k, const void *v, const int32_t *kv_len,
+                   const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, int n_sink,
+                   int n_stream, float scale, const dsa_decode_shape *shape, void *out,
+                   float *lse, DecodeArgs *args, size_t *part_floats) {
+  int st = check_decode_shape(shape);
+  if (st) return st;
+  if (max_sel < 0 || n_sink < 0 || n_stream < 0)
+    return fail(DSA_ERR_INVALID_ARG, "max_sel, n_sink and n_stream must be >= 0");
+  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "scale is not finite");
+  const int R = (shape->H_q / shape->H_kv) * shape->T_q;
+  if (R * shape->D > 4096)
+    return fail(DSA_ERR_UNSUPPORTED, "(H_q/H_kv)*T_q*D = %d > 4096 rows*dims per KV head", R * shape->D);
+  if (shape->dtype == DSA_BF16_FP8KV && R > 16)
+    return fail(DSA_ERR_UNSUPPORTED, "FP8 keys and values: (H_q/H_kv)*T_q = %d > 16", R);
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
+    return fail(DSA_ERR_ALIGNMENT, "q, k, v and out must be non-NULL and 16-byte aligned");
+  if (!aligned(kv_len, 4) || !aligned(sel_cnt, 4) || (max_sel > 0 && !aligned(sel_idx, 4)))
+    return fail(DSA_ERR_ALIGNMENT, "kv_len, sel_idx and sel_cnt must be non-NULL and 4-byte aligned");
+  if (lse && !aligned(lse, 4)) return fail(DSA_ERR_ALIGNMENT, "lse must be 4-byte aligned");
+  const long a_max = attended_max(shape, max_sel, n_sink, n_stream);
+  if (a_max > 0x7fffffffL) return fail(DSA_ERR_INVALID_ARG, "attended set too large");
+  const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
+  if (plan.n_split > 65535) return fail(DSA_ERR_INVALID_ARG, "too many splits (%d)", plan.n_split);
+  DecodeArgs &a = *args;
+  a = DecodeArgs{};
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.kv_len = kv_len;
+  a.sel_idx = sel_idx;
+  a.sel_cnt = sel_cnt;
+  a.max_sel = max_sel;
+  a.n_sink = n_sink;
+  a.n_stream = n_stream;
+  a.scale = scale;
+  a.B = shape->B;
+  a.T_max = shape->T_max;
+  a.T_q = shape->T_q;
+  a.H_q = shape->H_q;
+  a.H_kv = shape->H_kv;
+  a.D = shape->D;
+  a.dtype = shape->dtype;
+  a.n_split = plan.n_split;
+  a.keys_per_split = plan.keys_per_split;
+  a.cluster = plan.cluster;
+  a.part = nullptr;
+  a.out = out;
+  a.lse = lse;
+  *part_floats = decode_ws_floats(plan, shape->B, shape->T_q, shape->H_q, shape->D);
+  return DSA_OK;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -242,55 +298,16 @@ int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_
                        int n_stream, float scale, const dsa_decode_shape *shape, void *out,
                        float *lse, void *ws, size_t ws_bytes, void *stream) {
   clear_error();
-  int st = check_decode_shape(shape);
+  DecodeArgs a{};
+  size_t nf = 0;
+  int st = decode_prepare(q, k, v, kv_len, sel_idx, sel_cnt, max_sel, n_sink, n_stream, scale,
+                          shape, out, lse, &a, &nf);
   if (st) return st;
-  if (max_sel < 0 || n_sink < 0 || n_stream < 0)
-    return fail(DSA_ERR_INVALID_ARG, "max_sel, n_sink and n_stream must be >= 0");
-  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "scale is not finite");
-  const int R = (shape->H_q / shape->H_kv) * shape->T_q;
-  if (R * shape->D > 4096)
-    return fail(DSA_ERR_UNSUPPORTED, "(H_q/H_kv)*T_q*D = %d > 4096 rows*dims per KV head", R * shape->D);
-  if (shape->dtype == DSA_BF16_FP8KV && R > 16)
-    return fail(DSA_ERR_UNSUPPORTED, "FP8 keys and values: (H_q/H_kv)*T_q = %d > 16", R);
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
-    return fail(DSA_ERR_ALIGNMENT, "q, k, v and out must be non-NULL and 16-byte aligned");
-  if (!aligned(kv_len, 4) || !aligned(sel_cnt, 4) || (max_sel > 0 && !aligned(sel_idx, 4)))
-    return fail(DSA_ERR_ALIGNMENT, "kv_len, sel_idx and sel_cnt must be non-NULL and 4-byte aligned");
-  if (lse && !aligned(lse, 4)) return fail(DSA_ERR_ALIGNMENT, "lse must be 4-byte aligned");
-  const long a_max = attended_max(shape, max_sel, n_sink, n_stream);
-  if (a_max > 0x7fffffffL) return fail(DSA_ERR_INVALID_ARG, "attended set too large");
-  const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
-  if (plan.n_split > 65535) return fail(DSA_ERR_INVALID_ARG, "too many splits (%d)", plan.n_split);
-  const size_t nf = decode_ws_floats(plan, shape->B, shape->T_q, shape->H_q, shape->D);
   Carve cv(ws);
-  float *part = nf ? cv.take<float>(nf) : nullptr;
+  a.part = nf ? cv.take<float>(nf) : nullptr;
   if (ws_bytes < cv.bytes() || (nf && !aligned(ws, 16)))
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu",
                 cv.bytes(), ws_bytes);
-  DecodeArgs a{};
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.kv_len = kv_len;
-  a.sel_idx = sel_idx;
-  a.sel_cnt = sel_cnt;
-  a.max_sel = max_sel;
-  a.n_sink = n_sink;
-  a.n_stream = n_stream;
-  a.scale = scale;
-  a.B = shape->B;
-  a.T_max = shape->T_max;
-  a.T_q = shape->T_q;
-  a.H_q = shape->H_q;
-  a.H_kv = shape->H_kv;
-  a.D = shape->D;
-  a.dtype = shape->dtype;
-  a.n_split = plan.n_split;
-  a.keys_per_split = plan.keys_per_split;
-  a.cluster = plan.cluster;
-  a.part = part;
-  a.out = out;
-  a.lse = lse;
   cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return DSA_OK;

@@ -13,8 +13,11 @@
 // holds kDecodeStaticScratchBytes of it until the process exits.  Host code must not
 // hand the array's name to a kernel (on the host it is only a stand-in symbol);
 // the first call on each device looks up the device address with
-// cudaGetSymbolAddress while that device is current and caches it.
-#include <cmath>
+// cudaGetSymbolAddress while that device is current and caches it for that device's
+// context.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "api_common.h"
@@ -29,9 +32,46 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) float g_decode_scratch[kDecodeStaticScratchBytes / sizeof(float)];
 
 std::mutex g_scratch_mu;
-float *g_scratch_ptr[kMaxDevices] = {};
 
-// Device address of the array on the current device (looked up once per device).
+// The address is valid for one CUDA context: a cudaDeviceReset (by the host program or
+// another library) destroys the primary context and unloads this module's copy of the
+// array, and the next context may place it elsewhere.  So each device's cached address
+// is tagged with the unique id of the context it was looked up in (cuCtxGetId) and
+// looked up again when the current context's id differs.
+struct ScratchSlot {
+  unsigned long long ctx_id;
+  float *ptr;
+};
+ScratchSlot g_slot[kMaxDevices] = {};
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext *);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long *);
+
+// id of the calling thread's current context; false if there is none or the driver
+// does not say
+bool current_ctx_id(unsigned long long *id) {
+  static CtxGetCurrentFn get_cur = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_cur = reinterpret_cast<CtxGetCurrentFn>(p);
+    p = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess && q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  });
+  if (!get_cur || !get_id) return false;
+  CUcontext c = nullptr;
+  if (get_cur(&c) != CUDA_SUCCESS || c == nullptr) return false;
+  return get_id(c, id) == CUDA_SUCCESS;
+}
+
+// Device address of the array in the current device's current context: looked up with
+// cudaGetSymbolAddress on the first call in a context, cached after that.
 int static_scratch(float **out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -39,13 +79,18 @@ int static_scratch(float **out) {
   if (dev < 0 || dev >= kMaxDevices)
     return fail(DSA_ERR_INVALID_ARG, "device ordinal %d outside [0, %d)", dev, kMaxDevices);
   std::lock_guard<std::mutex> lk(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void *p = nullptr;
-    e = cudaGetSymbolAddress(&p, g_decode_scratch);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static decode scratch");
-    g_scratch_ptr[dev] = static_cast<float *>(p);
+  unsigned long long id = 0;
+  if (g_slot[dev].ptr && current_ctx_id(&id) && id == g_slot[dev].ctx_id) {
+    *out = g_slot[dev].ptr;
+    return DSA_OK;
   }
-  *out = g_scratch_ptr[dev];
+  void *p = nullptr;
+  e = cudaGetSymbolAddress(&p, g_decode_scratch);   // also makes the primary context current
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress of the static decode scratch");
+  g_slot[dev].ptr = static_cast<float *>(p);
+  g_slot[dev].ctx_id = current_ctx_id(&id) ? id : 0ull;   // 0: not cached, look up next time
+  if (!g_slot[dev].ctx_id) g_slot[dev].ptr = nullptr;
+  *out = static_cast<float *>(p);
   return DSA_OK;
 }
 
@@ -61,53 +106,21 @@ int sparse_attn_decode_noalloc(const void *q, const void *k, const void *v,
                                const int32_t *sel_cnt, int max_sel, int n_sink, int n_stream,
                                float scale, const dsa_decode_shape *shape, void *out, float *lse,
                                void *stream) {
-  size_t need = 0;
-  // validates the shape and sizes and gives the scratch the call needs
-  int st = sparse_attn_decode_workspace(shape, max_sel, n_sink, n_stream, &need);
+  clear_error();
+  DecodeArgs a{};
+  size_t nf = 0;
+  // the same checks and arguments as sparse_attn_decode; only the partials differ
+  int st = decode_prepare(q, k, v, kv_len, sel_idx, sel_cnt, max_sel, n_sink, n_stream, scale,
+                          shape, out, lse, &a, &nf);
   if (st) return st;
-  if (need > kDecodeStaticScratchBytes)
+  Carve cv(nullptr);
+  if (nf) cv.take<float>(nf);
+  if (cv.bytes() > kDecodeStaticScratchBytes)
     return fail(DSA_ERR_WORKSPACE,
                 "this decode needs %zu bytes of scratch but the built-in array holds %zu; "
                 "call sparse_attn_decode with a caller-owned workspace instead",
-                need, kDecodeStaticScratchBytes);
-  if (!std::isfinite(scale)) return fail(DSA_ERR_INVALID_ARG, "scale is not finite");
-  const int R = (shape->H_q / shape->H_kv) * shape->T_q;
-  if (R * shape->D > 4096)
-    return fail(DSA_ERR_UNSUPPORTED, "(H_q/H_kv)*T_q*D = %d > 4096 rows*dims per KV head", R * shape->D);
-  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(out, 16))
-    return fail(DSA_ERR_ALIGNMENT, "q, k, v and out must be non-NULL and 16-byte aligned");
-  if (!aligned(kv_len, 4) || !aligned(sel_cnt, 4) || (max_sel > 0 && !aligned(sel_idx, 4)))
-    return fail(DSA_ERR_ALIGNMENT, "kv_len, sel_idx and sel_cnt must be non-NULL and 4-byte aligned");
-  if (lse && !aligned(lse, 4)) return fail(DSA_ERR_ALIGNMENT, "lse must be 4-byte aligned");
-  float *part = nullptr;
-  if ((st = static_scratch(&part))) return st;
-  const long a_max = static_cast<long>(n_sink < shape->T_max ? n_sink : shape->T_max) + max_sel +
-                     (n_stream < shape->T_max ? n_stream : shape->T_max);
-  const DecodePlan plan = decode_plan(shape->B, shape->H_kv, R, shape->D, shape->dtype, static_cast<int>(a_max));
-  DecodeArgs a{};
-  a.q = q;
-  a.k = k;
-  a.v = v;
-  a.kv_len = kv_len;
-  a.sel_idx = sel_idx;
-  a.sel_cnt = sel_cnt;
-  a.max_sel = max_sel;
-  a.n_sink = n_sink;
-  a.n_stream = n_stream;
-  a.scale = scale;
-  a.B = shape->B;
-  a.T_max = shape->T_max;
-  a.T_q = shape->T_q;
-  a.H_q = shape->H_q;
-  a.H_kv = shape->H_kv;
-  a.D = shape->D;
-  a.dtype = shape->dtype;
-  a.n_split = plan.n_split;
-  a.keys_per_split = plan.keys_per_split;
-  a.cluster = plan.cluster;
-  a.part = part;
-  a.out = out;
-  a.lse = lse;
+                cv.bytes(), kDecodeStaticScratchBytes);
+  if (nf && (st = static_scratch(&a.part))) return st;
   cudaError_t e = launch_decode(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "decode launch");
   return DSA_OK;
