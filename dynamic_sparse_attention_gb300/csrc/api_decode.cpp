@@ -254,6 +254,7 @@ int hip_select_cached(const void *q, const void *k, const int32_t *kv_len,
     ta.out_stride = cfg->keep[i];
     ta.dbg_idx = dbg ? dbg->stage_idx[i] : nullptr;
     ta.dbg_cnt = dbg ? dbg->stage_cnt[i] : nullptr;
+    ta.release_dependents = last;
     {
       ProfScope ps(kTopkNames[i], s);
       e = launch_stage_topk(ta, s);

@@ -13,6 +13,10 @@ constexpr unsigned kFull = 0xffffffffu;
 // it reads anything an earlier kernel wrote or writes anything an earlier kernel
 // reads.  A kernel launched the ordinary way returns from it at once.
 __device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+// Lets the next kernel of the stream (launched with launch_pdl or the same attribute)
+// start before this one finishes; it still waits in grid_dep_wait() for this grid's
+// results.
+__device__ __forceinline__ void grid_dep_release() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }

@@ -333,6 +333,7 @@ __global__ void __launch_bounds__(kTopkThreads) stage_topk_kernel(StageTopkArgs 
   __shared__ uint32_t s_hist[256];
   __shared__ uint32_t s_res[2];
   __shared__ int s_warp[NT / 32 + 1];
+  if (a.release_dependents) grid_dep_release();
   grid_dep_wait();
   const int b = blockIdx.x, tid = threadIdx.x;
   const InputRange ir = stage_input(a.kv_len, b, a.T_max, a.n_sink, a.n_stream, a.in_idx,
@@ -436,6 +437,7 @@ __global__ void __launch_bounds__(kFastNT) stage_topk_fast_kernel(StageTopkArgs 
   __shared__ uint32_t s_misc[8];   // 0 min, 1 max, 2 boundary bucket, 3 count above, 4 candidates
   __shared__ uint32_t s_hist8[256];
   __shared__ uint32_t s_res[2];
+  if (a.release_dependents) grid_dep_release();
   grid_dep_wait();
   const int b = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int i0 = tid * NPT;
@@ -780,6 +782,7 @@ cudaError_t launch_score_t(const StageScoreArgs &a, cudaStream_t s) {
 }  // namespace
 
 cudaError_t launch_stage_score(const StageScoreArgs &a, cudaStream_t s) {
+  if (stage_score_tc_ok(a)) return launch_stage_score_tc(a, s);
   if (a.dtype == DSA_BF16_FP8KV) return launch_score_t<uint16_t, Fp8E4M3, 128>(a, s);   // D = 128
   if (a.dtype == DSA_BF16) {
     return a.D == 128 ? launch_score_t<uint16_t, uint16_t, 128>(a, s)

@@ -45,6 +45,11 @@ struct StageScoreArgs {
   float *dbg_rho;         // [B, H_q, max_chunks] or NULL
 };
 cudaError_t launch_stage_score(const StageScoreArgs &a, cudaStream_t s);
+// the same scores with the tournament probes on the tensor cores (stage_score_tc.cu):
+// bf16 q and k, one query row, H_q / H_kv in {2, 4, 8}, H_kv <= 8, chunks of more
+// than four tokens
+bool stage_score_tc_ok(const StageScoreArgs &a);
+cudaError_t launch_stage_score_tc(const StageScoreArgs &a, cudaStream_t s);
 
 // Top-K chunks + assembly of the kept tokens.
 struct StageTopkArgs {
@@ -62,6 +67,9 @@ struct StageTopkArgs {
   int out_stride;         // >= K * L
   int32_t *dbg_idx;       // optional copy of out_idx (stride out_stride)
   int32_t *dbg_cnt;
+  // the selection's last kernel lets the next grid of the stream start at once (the
+  // decode gathers its sink and window keys meanwhile and waits for the list)
+  bool release_dependents;
 };
 cudaError_t launch_stage_topk(const StageTopkArgs &a, cudaStream_t s);
 
@@ -75,6 +83,7 @@ struct DecodeArgs {
   float scale;
   int B, T_max, T_q, H_q, H_kv, D, dtype;
   int n_split, keys_per_split;
+  int fix_per, sel_per;   // cluster path: sink / window keys and selected slots per CTA
   bool cluster;           // plan path (see DecodePlan)
   float *part;            // [B, n_split, T_q, H_q, D + 2]
   void *out;

@@ -129,6 +129,10 @@ int hip_select_workspace(const dsa_decode_shape *shape, const dsa_hip_cfg *cfg, 
  *   there are at most K), and concatenate their tokens in ascending order.
  * Outputs: sel_idx [B, keep[n_stages-1]] final token list ascending, -1 padded;
  *          sel_cnt [B] its length.  dbg may be NULL.
+ * The last kernel lets the next kernel of the stream start early (programmatic
+ * dependent launch); a kernel that takes that start still waits for this one before
+ * it reads sel_idx / sel_cnt (sparse_attn_decode does), and a kernel launched the
+ * ordinary way starts after this call completes, as usual.
  * Errors: INVALID_ARG / UNSUPPORTED for shapes and configs, ALIGNMENT for
  * NULL/misaligned pointers, WORKSPACE if ws_bytes is short, CUDA on launch. */
 int hip_select(const void *q, const void *k, const int32_t *kv_len,
@@ -172,6 +176,13 @@ int sparse_attn_decode_workspace(const dsa_decode_shape *shape, int max_sel, int
  * sel_idx [B, max_sel] int32, entries ascending and inside [n_sink, T-n_stream);
  * sel_cnt [B] (clamped to [0, max_sel]).  out has the dtype of q.  A row with an
  * empty A gets out = 0 and lse = -inf.
+ * Early start: the kernel is launched with programmatic stream serialization, so it
+ * may start while the previous kernel of the stream still runs if that kernel allows
+ * it (hip_select's last kernel does, at its start; ordinary kernels do not).  It then
+ * reads q, k, v and kv_len and scores the sink and window keys at once, and waits for
+ * the previous kernel before it reads sel_idx / sel_cnt or writes out / lse.  So a
+ * kernel that writes q, k, v or kv_len and releases its dependents early must not come
+ * right before this call on the stream.
  * Errors as for hip_select. */
 int sparse_attn_decode(const void *q, const void *k, const void *v, const int32_t *kv_len,
                        const int32_t *sel_idx, const int32_t *sel_cnt, int max_sel, int n_sink,
