@@ -10,7 +10,6 @@ namespace dsa {
 namespace {
 
 constexpr int kBlock = 64;
-constexpr int kDiagPerTile = 127;
 
 int check_prefill_shape(const dsa_prefill_shape *s) {
   if (!s) return fail(DSA_ERR_INVALID_ARG, "shape is NULL");
@@ -34,6 +33,8 @@ int check_vs_cfg(const dsa_prefill_shape *s, const dsa_vs_cfg *c) {
     return fail(DSA_ERR_INVALID_ARG, "n_slash=%d outside [0, S=%d]", c->n_slash, s->S);
   if (s->H_q / s->H_kv > 8)
     return fail(DSA_ERR_UNSUPPORTED, "H_q/H_kv=%d > 8 query heads per KV head", s->H_q / s->H_kv);
+  int st = vs_tc_check(s->D, s->H_q / s->H_kv);
+  if (st) return st;
   const long n_qblk = (s->S + kBlock - 1) / kBlock;
   const long conv_smem = (2 * ((n_qblk + 31) / 32) + n_qblk + c->n_vertical) * 4;
   if (conv_smem > 200 * 1024)
@@ -52,9 +53,12 @@ VsWs vs_layout(const dsa_prefill_shape *s, void *base) {
   VsWs w{};
   Carve cv(base);
   const int G = s->H_q / s->H_kv;
-  w.n_ktile = (s->S + kVsKeyTile - 1) / kVsKeyTile;
+  // row statistics: one partial per run of the first pass; diagonal partials: one set
+  // per tile of the second pass
+  const int tile0 = vs_tc_tile0(G), tile1 = vs_tc_tile1();
   int tps;
-  vs_plan(s->B, s->H_kv, w.n_ktile, &w.n_split, &tps);
+  vs_tc_plan(s->B, s->H_kv, (s->S + tile0 - 1) / tile0, &w.n_split, &tps);
+  w.n_ktile = (s->S + tile1 - 1) / tile1;
   const size_t rows = static_cast<size_t>(s->B) * s->H_kv * w.n_split * G * 64;
   w.part_m = cv.take<float>(rows);
   w.part_l = cv.take<float>(rows);
@@ -62,7 +66,7 @@ VsWs vs_layout(const dsa_prefill_shape *s, void *base) {
   w.row_l = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * 64);
   w.vsum = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * s->S);
   w.ssum = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * s->S);
-  w.slash_part = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * w.n_ktile * kDiagPerTile);
+  w.slash_part = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * w.n_ktile * vs_tc_diag());
   w.bytes = cv.bytes();
   return w;
 }
@@ -278,6 +282,7 @@ int vs_index_build(const void *q, const void *k, const dsa_prefill_shape *shape,
   if (ws_bytes < need.bytes || !aligned(ws, 16))
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu",
                 need.bytes, ws_bytes);
+  if ((st = vs_tc_ready())) return st;
   const VsWs w = vs_layout(shape, ws);
   cudaError_t e = run_vs(q, k, shape, cfg, vertical, slash, blk_cnt, blk_idx, col_cnt, col_idx, dbg,
                          w, HeadSet{}, static_cast<cudaStream_t>(stream));
@@ -410,6 +415,7 @@ int mixed_index_build(const void *q, const void *k, const dsa_prefill_shape *sha
   if (ws_bytes < need || (need > 0 && !aligned(ws, 16)))
     return fail(DSA_ERR_WORKSPACE, "workspace of %zu bytes (16-byte aligned) needed, got %zu", need,
                 ws_bytes);
+  if (any_vs && (st = vs_tc_ready())) return st;
   const MixedWs w = mixed_layout(shape, cfg, ws);
   const int n_qblk = (shape->S + kBlock - 1) / kBlock;
   cudaStream_t s = static_cast<cudaStream_t>(stream);

@@ -2,6 +2,8 @@
 // Arguments are validated by the caller; launchers only enqueue work.
 #pragma once
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -9,6 +11,12 @@
 #include "dsa.h"
 
 namespace dsa {
+
+// The driver's tensor-map encoder (NULL if the driver offers none), and a 4-D TMA map
+// (d, head, position, batch) of a [B, S, H, D] bf16 tensor with a box of 64 d x 1 head
+// x `rows` positions, 128-byte swizzle (prefill_tc.cu).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+bool make_bshd_map(CUtensorMap *m, const void *base, int D, int H, int S, int B, int rows);
 
 // Launch with programmatic stream serialization allowed: the grid may start while
 // the stream's previous kernel drains (its CTAs then wait in grid_dep_wait()).
@@ -136,14 +144,31 @@ struct VsArgs {
   float *row_m, *row_l;       // [B, H_q, 64] final row max / sum (base-2 logits)
   float *part_m, *part_l;     // [B, H_kv, n_split, G*64] per key-split row stats
   float *vsum, *ssum;         // [B, H_q, S] column sums / diagonal sums
-  float *slash_part;          // [B, H_q, n_ktile, 127] per key-tile diagonal sums
+  float *slash_part;          // [B, H_q, n_ktile, vs_tc_diag()] per key-tile diagonal sums
   int n_ktile;
   HeadSet heads;              // heads whose lists are written (the estimate covers all)
 };
 cudaError_t launch_vs_index(const VsArgs &a, cudaStream_t s);
-constexpr int kVsKeyTile = 64;
-// number of key splits of the estimate passes (shared by workspace query and launch)
-void vs_plan(int B, int H_kv, int n_ktile, int *n_split, int *tiles_per_split);
+// The estimate's two passes on tcgen05 (vs_tc.cu): row statistics, then column sums and
+// per-128-key-tile diagonal partials (vs_tc_diag() offsets each), then their combine.
+struct VsTcLaunch {
+  const void *q, *k;
+  int B, S, H_q, H_kv, D, last_q;
+  float scale;
+  float *part_m, *part_l;      // [B, H_kv, n_split0, G * 64]
+  float *row_m, *row_l;        // [B, H_q, 64]
+  float *vsum, *ssum;          // [B, H_q, S]
+  float *slash_part;           // [B, H_q, n_ktile1, vs_tc_diag()]
+  HeadSet heads;               // heads whose slash sums are combined
+};
+int vs_tc_check(int D, int G);   // shape limits: DSA_OK or a status with the reason
+int vs_tc_ready();               // the driver's tensor-map encoder is there (launch time)
+int vs_tc_tile0(int G);          // keys per tile of the row-statistics pass
+int vs_tc_tile1();               // keys per tile of the sums pass
+int vs_tc_diag();                // diagonal partials per sums-pass tile (floats)
+void vs_tc_plan(int B, int H_kv, int n_ktile, int *n_split, int *tiles_per_split);
+cudaError_t launch_vs_tc(const VsTcLaunch &l, cudaStream_t s);
+int vs_tc_device_error();        // the estimate's device error word (read and cleared)
 
 // Sparse prefill attention over tile / column lists.
 struct PrefillArgs {

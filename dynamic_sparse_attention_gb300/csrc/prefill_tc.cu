@@ -650,9 +650,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   if (tid == 0 && *abort_flag) atomicExch(&g_prefill_tc_error, 1);
 }
 
+}  // namespace
+
 // ------------------------------------------------------------------ host side
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
   std::call_once(once, [] {
@@ -667,8 +669,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // 4-D view (d, head, position, batch) of a bshd bf16 tensor; box = 64 d x 1 x rows x 1
-bool make_map(CUtensorMap *m, const void *base, int D, int H, int S, int B, int rows) {
-  auto enc = encode_fn();
+bool make_bshd_map(CUtensorMap *m, const void *base, int D, int H, int S, int B, int rows) {
+  auto enc = tensor_map_encoder();
   if (!enc) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(S), static_cast<cuuint64_t>(B)};
@@ -681,13 +683,15 @@ bool make_map(CUtensorMap *m, const void *base, int D, int H, int S, int B, int 
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace {
+
 template <int D>
 cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!make_map(&a.tq, pa.q, D, pa.H_q, pa.S, pa.B, kRowsQ) ||
-      !make_map(&a.tk, pa.k, D, pa.H_kv, pa.S, pa.B, kBlk) ||
-      !make_map(&a.tv, pa.v, D, pa.H_kv, pa.S, pa.B, kBlk))
+  if (!make_bshd_map(&a.tq, pa.q, D, pa.H_q, pa.S, pa.B, kRowsQ) ||
+      !make_bshd_map(&a.tk, pa.k, D, pa.H_kv, pa.S, pa.B, kBlk) ||
+      !make_bshd_map(&a.tv, pa.v, D, pa.H_kv, pa.S, pa.B, kBlk))
     return cudaErrorInvalidValue;
   a.k = static_cast<const uint16_t *>(pa.k);
   a.v = static_cast<const uint16_t *>(pa.v);
@@ -735,7 +739,7 @@ int prefill_tc_check(const PrefillArgs &a) {
                                  : Layout<64>::bytes((n_qblk + 31) / 32);
   if (smem > 227 * 1024)
     return fail(DSA_ERR_UNSUPPORTED, "S=%d: %zu bytes of shared memory per CTA > 227 KiB", a.S, smem);
-  if (encode_fn() == nullptr)
+  if (tensor_map_encoder() == nullptr)
     return fail(DSA_ERR_UNSUPPORTED, "the driver offers no cuTensorMapEncodeTiled entry point");
   return DSA_OK;
 }
@@ -754,6 +758,8 @@ extern "C" int dsa_device_error(int *code) {
   cudaError_t e = cudaMemcpyFromSymbol(&v, g_prefill_tc_error, sizeof(int));
   if (e == cudaSuccess) e = cudaMemcpyToSymbol(g_prefill_tc_error, &zero, sizeof(int));
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
-  *code = v;
+  const int w = vs_tc_device_error();   // the vertical-slash estimate's word
+  if (w < 0) return fail(DSA_ERR_CUDA, "reading the estimate's device error word");
+  *code = v | (w << 1);
   return DSA_OK;
 }

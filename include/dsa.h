@@ -417,11 +417,13 @@ int dsa_profile_collect(dsa_kernel_stat *out, int max_out, int *n_out);
 
 /* ------------------------------------------------------------------ diagnostics */
 
-/* Every wait inside the tensor-core prefill is bounded; a CTA that gives up stops
- * issuing work, frees its resources, writes zero output and sets a device error
- * word.  dsa_device_error copies that word to *code (0 = none) and clears it.  It
- * synchronises with the device (cudaMemcpyFromSymbol); call it between steps, not on
- * a hot path.  Not a source-page operation. */
+/* Every wait inside the tensor-core kernels (the prefill attention and the two passes
+ * of the vertical-slash estimate) is bounded; a CTA that gives up stops issuing work,
+ * frees its resources and sets a device error word (the prefill CTA also writes zero
+ * output).  dsa_device_error copies the words to *code (0 = none; bit 0: the prefill
+ * attention, bit 1: the estimate) and clears them.  It synchronises with the device
+ * (cudaMemcpyFromSymbol); call it between steps, not on a hot path.  Not a
+ * source-page operation. */
 int dsa_device_error(int *code);
 
 /* ------------------------------------------------------------------ helpers */
