@@ -59,7 +59,7 @@ VsWs vs_layout(const dsa_prefill_shape *s, void *base) {
   int tps;
   vs_tc_plan(s->B, s->H_kv, (s->S + tile0 - 1) / tile0, &w.n_split, &tps);
   w.n_ktile = (s->S + tile1 - 1) / tile1;
-  const size_t rows = static_cast<size_t>(s->B) * s->H_kv * w.n_split * G * 64;
+  const size_t rows = static_cast<size_t>(s->B) * s->H_kv * w.n_split * vs_tc_khalves(G) * G * 64;
   w.part_m = cv.take<float>(rows);
   w.part_l = cv.take<float>(rows);
   w.row_m = cv.take<float>(static_cast<size_t>(s->B) * s->H_q * 64);

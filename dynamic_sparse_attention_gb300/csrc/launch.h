@@ -155,7 +155,7 @@ struct VsTcLaunch {
   const void *q, *k;
   int B, S, H_q, H_kv, D, last_q;
   float scale;
-  float *part_m, *part_l;      // [B, H_kv, n_split0, G * 64]
+  float *part_m, *part_l;      // [B, H_kv, n_split0 * khalves, G * 64]
   float *row_m, *row_l;        // [B, H_q, 64]
   float *vsum, *ssum;          // [B, H_q, S]
   float *slash_part;           // [B, H_q, n_ktile1, vs_tc_diag()]
@@ -164,6 +164,7 @@ struct VsTcLaunch {
 int vs_tc_check(int D, int G);   // shape limits: DSA_OK or a status with the reason
 int vs_tc_ready();               // the driver's tensor-map encoder is there (launch time)
 int vs_tc_tile0(int G);          // keys per tile of the row-statistics pass
+int vs_tc_khalves(int G);        // row-statistics partials per key run (key parts)
 int vs_tc_tile1();               // keys per tile of the sums pass
 int vs_tc_diag();                // diagonal partials per sums-pass tile (floats)
 void vs_tc_plan(int B, int H_kv, int n_ktile, int *n_split, int *tiles_per_split);

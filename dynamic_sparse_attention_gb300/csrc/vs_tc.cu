@@ -61,7 +61,7 @@ struct VsTcArgs {
   int kt;                 // keys per tile of this pass
   int n_ktile, tiles_per_split, n_split;
   float sl2;
-  float *part_m, *part_l;           // pass 0 out: [B, H_kv, n_split, G * 64]
+  float *part_m, *part_l;           // pass 0 out: [B, H_kv, n_split * khalves, G * 64]
   const float *row_m, *row_l;       // pass 1 in: [B, H_q, 64] (base-2 logits)
   float *vsum;                      // pass 1 out: [B, H_q, S]
   float *slash_part;                // pass 1 out: [B, H_q, n_ktile, kDiag1, 2 row halves]
@@ -72,7 +72,7 @@ struct VsTcArgs {
 // the key ring and nph shrink, in that order, until everything fits.
 struct TcLayout {
   uint32_t halves, q_half, k_half, k_stage, stages, nph;
-  uint32_t oQ, oK, oBar, oMisc, oC, oP, total;
+  uint32_t oQ, oK, oBar, oMisc, oC, oP, oV, total;
   __host__ __device__ TcLayout(int G, int D, int kt, int pass) {
     halves = D / 64;
     const int slots = pass == 0 ? ((G + 1) / 2) * 2 : G;   // pass 0 pads to pairs of heads
@@ -80,7 +80,7 @@ struct TcLayout {
     k_half = static_cast<uint32_t>(kt) * 128;
     k_stage = halves * k_half;
     const uint32_t p_head = kBoxRows * kTile1 * 4;
-    const uint32_t fixed = halves * q_half + 64 * 8 + 64 + static_cast<uint32_t>(G) * kBoxRows * 4 + 1024;
+    const uint32_t fixed = halves * q_half + 64 * 8 + 64 + static_cast<uint32_t>(G) * kBoxRows * 4 + 4 * kTile1 * 4 + 1024;
     const uint32_t budget = 227u * 1024u;
     stages = kMaxStages;
     nph = pass == 1 ? (G >= 2 ? 2u : 1u) : 0u;
@@ -96,7 +96,8 @@ struct TcLayout {
     oMisc = oBar + 64 * 8;
     oC = oMisc + 64;                                        // pass 1: c per (head, row)
     oP = oC + static_cast<uint32_t>(G) * kBoxRows * 4;      // pass 1: probabilities
-    total = oP + nph * p_head;
+    oV = oP + nph * p_head;                                 // pass 1: [2 heads][2 row halves][128] column sums
+    total = oV + (pass == 1 ? 4u * kTile1 * 4u : 0u);
   }
 };
 
@@ -139,7 +140,7 @@ __device__ __forceinline__ float ex2(float x) {
 }
 
 template <int PASS>
-__global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const __grid_constant__ VsTcArgs a) {
+__global__ void __launch_bounds__(640, 1) vs_tc_kernel(const __grid_constant__ VsTcArgs a) {
   const TcLayout L(a.G, a.D, a.kt, PASS);
   extern __shared__ unsigned char smem_raw[];
   unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -276,7 +277,11 @@ __global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const _
     const int quarter = warp & 3;   // TMEM lanes this warp may access
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     if (PASS == 0) {
-      const int slot = e >> 2;                      // head pair of this warp
+      // warp e: head pair slot (e >> 2) % n_slot, key half e / (4 n_slot) of every tile
+      const int n_slot = (G + 1) / 2;
+      const int slot = (e >> 2) % n_slot;
+      const int kh = e / (4 * n_slot), nkh = n_epi / (4 * n_slot);
+      const int kw = a.kt / nkh;                    // keys of a tile this warp reads
       const int row = quarter * 32 + lane;          // row of the pair
       const int hs = 2 * slot + (row >> 6), br = row & 63;
       const int pos = S - kBoxRows + br;            // query position of the row
@@ -286,10 +291,10 @@ __global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const _
         const int buf = i % n_buf;
         if (!warp_wait(wt, &s_full[buf], (i / n_buf) & 1)) break;
         tc_fence_after();
-        const int j0 = (t_begin + i) * a.kt;
-        for (int c0 = 0; c0 < a.kt; c0 += 32) {
+        const int j0 = (t_begin + i) * a.kt + kh * kw;
+        for (int c0 = 0; c0 < kw; c0 += 32) {
           uint32_t r[32];
-          tmem_ld32(tl + static_cast<uint32_t>(buf) * buf_cols + static_cast<uint32_t>(slot * a.kt + c0), r);
+          tmem_ld32(tl + static_cast<uint32_t>(buf) * buf_cols + static_cast<uint32_t>(slot * a.kt + kh * kw + c0), r);
           tmem_wait_ld();
           float v[32];
           float mx = -INFINITY;
@@ -317,26 +322,29 @@ __global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const _
       }
       if (row_ok && !*abort_flag) {
         const int ir = br - (kBoxRows - a.r_q);
-        const size_t o = ((static_cast<size_t>(b) * a.H_kv + g) * a.n_split + split) * (G * kBoxRows) +
-                         hs * kBoxRows + ir;
+        // one partial per (run, key half): the combine kernel takes n_split * nkh of them
+        const size_t o = ((static_cast<size_t>(b) * a.H_kv + g) * a.n_split * nkh + split * nkh + kh) *
+                             (G * kBoxRows) + hs * kBoxRows + ir;
         a.part_m[o] = m_run;
         a.part_l[o] = l_run;
       }
     } else {
-      // One thread per key of the tile (four warps per head, one per lane quarter); the
-      // tile's heads go in rounds of nph, head hs = round * nph + hp handled by the warps
-      // with hp = e >> 2.  Per round: the probabilities to shared memory (row br, key jl)
-      // and the column sums to vsum; one barrier; each thread sums whole diagonals
-      // u = br - jl + 127 of the round's heads (a warp reads 32 consecutive addresses per
-      // row); one barrier before the buffer is written again.  The bounded wait for the
-      // tile's scores is followed by a barrier and a shared abort check, so the epilogue
-      // warps take every barrier together or leave together (only they write epi_abort,
-      // and only before that barrier).
+      // One thread per key of the tile and half of a head's 64 rows (eight warps per
+      // head: lane quarter x row half); the tile's heads go in rounds of nph, head
+      // hs = round * nph + hp handled by the warps with hp = (e >> 2) & 1.  Per round:
+      // the probabilities to shared memory (row br, key jl) and the half column sums;
+      // one barrier; the column sums to vsum (the two halves in order) and each thread
+      // sums half-diagonals u = br - jl + 127 of the round's heads (a warp reads 32
+      // consecutive addresses per row); one barrier before the buffer is written again.
+      // The bounded wait for the tile's scores is followed by a barrier and a shared
+      // abort check, so the epilogue warps take every barrier together or leave together
+      // (only they write epi_abort, and only before that barrier).
       const int nph = static_cast<int>(L.nph);
-      const int hp = e >> 2;
+      const int hp = (e >> 2) & 1, rh = e >> 3;
       const int jl = quarter * 32 + lane;    // key of the tile owned by this thread
       const float *cst = reinterpret_cast<const float *>(sm + L.oC);
       float *P = reinterpret_cast<float *>(sm + L.oP);
+      float *s_vs = reinterpret_cast<float *>(sm + L.oV);
       const int n_epi_thr = n_epi * 32;
       const int et = tid - 4 * 32;           // epilogue thread index
       const int n_round = (G + nph - 1) / nph;
@@ -351,18 +359,16 @@ __global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const _
         for (int rd = 0; rd < n_round; ++rd) {
           const int hs = rd * nph + hp;
           if (hp < nph && hs < G) {
-            uint32_t r[64];
-            const uint32_t col = tl + static_cast<uint32_t>(buf) * buf_cols + static_cast<uint32_t>(hs * 64);
-            tmem_ld32(col, r);
-            tmem_ld32(col + 32, r + 32);
+            uint32_t r[32];
+            tmem_ld32(tl + static_cast<uint32_t>(buf) * buf_cols + static_cast<uint32_t>(hs * 64 + 32 * rh), r);
             tmem_wait_ld();
-            const float4 *c4 = reinterpret_cast<const float4 *>(cst + hs * kBoxRows);
-            float *Ph = P + hp * kBoxRows * kTile1 + jl;
+            const float4 *c4 = reinterpret_cast<const float4 *>(cst + hs * kBoxRows + 32 * rh);
+            float *Ph = P + hp * kBoxRows * kTile1 + 32 * rh * kTile1 + jl;
             // row br attends key j iff br is an estimate row and j <= S - 64 + br
-            const int br_lo = max(kBoxRows - a.r_q, j - (S - kBoxRows));
+            const int br_lo = max(kBoxRows - a.r_q, j - (S - kBoxRows)) - 32 * rh;
             float vs = 0.f;
 #pragma unroll
-            for (int b4 = 0; b4 < kBoxRows / 4; ++b4) {
+            for (int b4 = 0; b4 < 8; ++b4) {
               const float4 cc = c4[b4];
               const float cv[4] = {cc.x, cc.y, cc.z, cc.w};
 #pragma unroll
@@ -373,7 +379,7 @@ __global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const _
                 Ph[br * kTile1] = pr;
               }
             }
-            if (j < S) a.vsum[(static_cast<size_t>(b) * a.H_q + g * G + hs) * S + j] = vs;
+            s_vs[(hp * 2 + rh) * kTile1 + jl] = vs;
           }
           if (rd == n_round - 1) {
             // every score of the tile is in registers: its TMEM buffer is free
@@ -382,9 +388,16 @@ __global__ void __launch_bounds__(PASS == 0 ? 640 : 384, 1) vs_tc_kernel(const _
             if (lane == 0) mbar_arrive(&s_empty[buf]);
           }
           named_bar_sync(1, n_epi_thr);
+          const int n_h = min(nph, G - rd * nph);
+          for (int x = et; x < n_h * kTile1; x += n_epi_thr) {
+            const int sl = x / kTile1, k = x - sl * kTile1;
+            const int jj = t * kTile1 + k;
+            if (jj < S)
+              a.vsum[(static_cast<size_t>(b) * a.H_q + g * G + rd * nph + sl) * S + jj] =
+                  s_vs[(sl * 2) * kTile1 + k] + s_vs[(sl * 2 + 1) * kTile1 + k];
+          }
           // one item = one diagonal u of one head, over one half of the rows (two
           // partials per diagonal; the combine kernel adds them)
-          const int n_h = min(nph, G - rd * nph);
           for (int x = et; x < n_h * 2 * kDiag1; x += n_epi_thr) {
             const int sl = x / (2 * kDiag1), rem = x - sl * 2 * kDiag1;
             const int half = rem / kDiag1, u = rem - half * kDiag1;
@@ -468,6 +481,9 @@ __global__ void vs_slash_tc_kernel(float *ssum, const float *slash_part, int B, 
 }  // namespace
 
 int vs_tc_tile0(int G) { return G <= 4 ? 128 : 64; }
+// warps sharing a row in the row-statistics pass, each on its part of every tile's keys
+// (two per row measured slower than one: 142 vs 133 us at 128K)
+int vs_tc_khalves(int) { return 1; }
 int vs_tc_tile1() { return kTile1; }
 int vs_tc_diag() { return 2 * kDiag1; }
 
@@ -522,7 +538,7 @@ cudaError_t launch_vs_tc(const VsTcLaunch &l, cudaStream_t s) {
     const TcLayout lay(G, l.D, a.kt, pass);
     // at least 116 KB, so that one CTA (and its 512 TMEM columns) holds an SM
     const size_t smem = lay.total + 1024 > 116 * 1024 ? lay.total + 1024 : 116 * 1024;
-    const int epi = pass == 0 ? 4 * ((G + 1) / 2) : 8;
+    const int epi = pass == 0 ? 4 * ((G + 1) / 2) * vs_tc_khalves(G) : 16;
     const int threads = 32 * (4 + epi);
     dim3 grid(a.n_split, l.H_kv, l.B);
     if (pass == 0) {
@@ -536,7 +552,7 @@ cudaError_t launch_vs_tc(const VsTcLaunch &l, cudaStream_t s) {
       const int total = l.B * l.H_q * kBoxRows;
       ProfScope ps2("vs_combine_rowstats", s);
       vs_tc_stats_kernel<<<(total + 255) / 256, 256, 0, s>>>(l.part_m, l.part_l, l.row_m, l.row_l, l.B,
-                                                             l.H_q, l.H_kv, r_q, a.n_split);
+                                                             l.H_q, l.H_kv, r_q, a.n_split * vs_tc_khalves(G));
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     } else {
       auto kern = vs_tc_kernel<1>;
