@@ -29,6 +29,7 @@ from .binding import (  # noqa: F401
     profile_collect,
     profile_enable,
     refresh_mask,
+    set_wait_limit,
     sparse_attn_decode,
     sparse_attn_decode_noalloc,
     sparse_attn_decode_workspace_bytes,

@@ -109,6 +109,7 @@ _SIGNATURES = {
     "sparse_attn_decode_noalloc": (_c_int, [_vp, _vp, _vp, _vp, _vp, _vp, _c_int, _c_int, _c_int,
                                             ctypes.c_float, _vp, _vp, _vp, _vp]),
     "dsa_device_error": (_c_int, [ctypes.POINTER(_c_int)]),
+    "dsa_set_wait_limit": (_c_int, [ctypes.c_ulonglong]),
     "dsa_profile_enable": (_c_int, [_c_int]),
     "dsa_profile_collect": (_c_int, [_vp, _c_int, ctypes.POINTER(_c_int)]),
 }
@@ -120,6 +121,12 @@ def device_error() -> int:
     c = _c_int()
     _check("dsa_device_error", lib.dsa_device_error(ctypes.byref(c)))
     return c.value
+
+
+def set_wait_limit(ns: int = 0) -> None:
+    """Limit of the tensor-core kernels' bounded waits in nanoseconds (0: the default)."""
+    lib = load()
+    _check("dsa_set_wait_limit", lib.dsa_set_wait_limit(ctypes.c_ulonglong(ns)))
 
 
 def profile_enable(on: bool = True) -> None:

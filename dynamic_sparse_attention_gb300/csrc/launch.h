@@ -170,6 +170,9 @@ int vs_tc_diag();                // diagonal partials per sums-pass tile (floats
 void vs_tc_plan(int B, int H_kv, int n_ktile, int *n_split, int *tiles_per_split);
 cudaError_t launch_vs_tc(const VsTcLaunch &l, cudaStream_t s);
 int vs_tc_device_error();        // the estimate's device error word (read and cleared)
+// wait limits of the tensor-core kernels' bounded waits (0 on success)
+int vs_tc_set_wait_limit(unsigned long long ns);
+int prefill_tc_set_wait_limit(unsigned long long ns);
 
 // Sparse prefill attention over tile / column lists.
 struct PrefillArgs {

@@ -80,6 +80,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 static __device__ int g_prefill_tc_error;   // sticky error word, read by dsa_device_error
 static __device__ int g_abort_epoch;         // launch epoch of a launch in which a CTA gave up
 constexpr uint64_t kWaitLimitNs = 500000000ull;
+// wait limit of the kernel's bounded waits (dsa_set_wait_limit; default kWaitLimitNs)
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
 
 struct TileMeta {
   int kind;          // 0: block tile (two 64-key list blocks), 1: gathered column tile
@@ -133,16 +135,18 @@ struct WaitCtx {
 __device__ __forceinline__ bool tc_wait(uint64_t *bar, uint32_t parity, const WaitCtx &w) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
+  const uint64_t limit = g_wait_limit_ns;
+  const uint32_t hint = limit < 20000ull ? static_cast<uint32_t>(limit) : 20000u;
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+    if (mbar_try_wait_hint(bar, parity, hint)) return true;
     if (*w.cta_abort) return false;
     if ((++spins & 7u) == 0u) {
       if (*reinterpret_cast<volatile int *>(&g_abort_epoch) == w.epoch) {
         *w.cta_abort = 1;
         return false;
       }
-      if (global_ns() - t0 > kWaitLimitNs) {
+      if (global_ns() - t0 > limit) {
         *w.cta_abort = 1;
         atomicExch(&g_abort_epoch, w.epoch);
         return false;
@@ -761,5 +765,20 @@ extern "C" int dsa_device_error(int *code) {
   const int w = vs_tc_device_error();   // the vertical-slash estimate's word
   if (w < 0) return fail(DSA_ERR_CUDA, "reading the estimate's device error word");
   *code = v | (w << 1);
+  return DSA_OK;
+}
+
+namespace dsa {
+int prefill_tc_set_wait_limit(unsigned long long ns) {
+  return cudaMemcpyToSymbol(g_wait_limit_ns, &ns, sizeof(ns)) == cudaSuccess ? 0 : -1;
+}
+}  // namespace dsa
+
+extern "C" int dsa_set_wait_limit(unsigned long long ns) {
+  using namespace dsa;
+  clear_error();
+  const unsigned long long v = ns ? ns : kWaitLimitNs;
+  if (prefill_tc_set_wait_limit(v) || vs_tc_set_wait_limit(v))
+    return fail(DSA_ERR_CUDA, "setting the wait limit of the tensor-core kernels");
   return DSA_OK;
 }

@@ -42,6 +42,8 @@
 namespace dsa {
 
 static __device__ int g_vs_tc_error;   // sticky error word, read by dsa_device_error
+// wait limit of the bounded waits (dsa_set_wait_limit; default half a second)
+static __device__ unsigned long long g_vs_wait_limit_ns = 500000000ull;
 
 namespace {
 
@@ -52,7 +54,6 @@ constexpr int kTile1 = 128;           // keys per tile in pass 1 (TMEM lanes)
 constexpr int kDiag1 = kTile1 + kBoxRows - 1;   // diagonals one pass-1 tile touches
 constexpr int kMaxStages = 3;         // key-tile ring (two where shared memory is short)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint64_t kWaitNs = 500000000ull;
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct VsTcArgs {
@@ -106,10 +107,12 @@ struct Waiter {
   __device__ bool operator()(uint64_t *bar, uint32_t parity) const {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
+    const uint64_t limit = g_vs_wait_limit_ns;
+    const uint32_t hint = limit < 20000ull ? static_cast<uint32_t>(limit) : 20000u;
     while (true) {
-      if (mbar_try_wait_hint(bar, parity, 20000u)) return true;
+      if (mbar_try_wait_hint(bar, parity, hint)) return true;
       if (*abort) return false;
-      if (global_ns() - t0 > kWaitNs) {
+      if (global_ns() - t0 > limit) {
         *abort = 1;
         return false;
       }
@@ -570,6 +573,10 @@ cudaError_t launch_vs_tc(const VsTcLaunch &l, cudaStream_t s) {
     }
   }
   return cudaSuccess;
+}
+
+int vs_tc_set_wait_limit(unsigned long long ns) {
+  return cudaMemcpyToSymbol(g_vs_wait_limit_ns, &ns, sizeof(ns)) == cudaSuccess ? 0 : -1;
 }
 
 int vs_tc_device_error() {

@@ -426,6 +426,13 @@ int dsa_profile_collect(dsa_kernel_stat *out, int max_out, int *n_out);
  * source-page operation. */
 int dsa_device_error(int *code);
 
+/* Sets the limit of those bounded waits to `ns` nanoseconds (0: back to the default of
+ * half a second) for every later launch; it synchronises (cudaMemcpyToSymbol).  A test
+ * aid: a limit of a few nanoseconds makes the waits run out, so that the give-up path
+ * (stop, drain, free, error word) can be exercised without any fault.  Not a
+ * source-page operation. */
+int dsa_set_wait_limit(unsigned long long ns);
+
 /* ------------------------------------------------------------------ helpers */
 
 const char *dsa_last_error(void);   /* last validation / launch message of this thread */
