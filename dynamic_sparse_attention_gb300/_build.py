@@ -18,6 +18,9 @@ CSRC = os.path.join(PKG, "csrc")
 LIBDIR = os.path.join(PKG, "_lib")
 OBJDIR = os.path.join(LIBDIR, "obj")
 LIB = os.path.join(LIBDIR, "libdsa.so")
+# the checked build: device-side input checks compiled in (-DDSA_CHECKS=1)
+OBJDIR_CHECKED = os.path.join(LIBDIR, "obj_checked")
+LIB_CHECKED = os.path.join(LIBDIR, "libdsa_checked.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMMON = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -49,17 +52,21 @@ def _stale(obj: str, src: str, newest_header: float) -> bool:
     return os.path.getmtime(src) > t or newest_header > t
 
 
-def build(verbose: bool = False, jobs: int | None = None, extra_flags=None) -> str:
-    """Compile (if needed) and return the path of libdsa.so."""
+def build(verbose: bool = False, jobs: int | None = None, extra_flags=None,
+          checked: bool = False) -> str:
+    """Compile (if needed) and return the path of libdsa.so (checked: libdsa_checked.so,
+    with the device-side input checks compiled in)."""
     nvcc = _nvcc()
-    os.makedirs(OBJDIR, exist_ok=True)
+    objdir = OBJDIR_CHECKED if checked else OBJDIR
+    lib = LIB_CHECKED if checked else LIB
+    os.makedirs(objdir, exist_ok=True)
     srcs = _sources()
     newest_header = max((os.path.getmtime(h) for h in _headers()), default=0.0)
-    flags = COMMON + list(extra_flags or [])
+    flags = COMMON + list(extra_flags or []) + (["-DDSA_CHECKS=1"] if checked else [])
     todo = []
     objs = []
     for src in srcs:
-        obj = os.path.join(OBJDIR, os.path.basename(src) + ".o")
+        obj = os.path.join(objdir, os.path.basename(src) + ".o")
         objs.append(obj)
         if _stale(obj, src, newest_header):
             todo.append((src, obj))
@@ -79,14 +86,14 @@ def build(verbose: bool = False, jobs: int | None = None, extra_flags=None) -> s
             for msg in ex.map(compile_one, todo):
                 if msg:
                     print(msg)
-    if todo or not os.path.exists(LIB):
-        tmp = LIB + ".tmp"
+    if todo or not os.path.exists(lib):
+        tmp = lib + ".tmp"
         cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
-            raise RuntimeError(f"link of libdsa.so failed:\n{r.stdout}\n{r.stderr}")
-        os.replace(tmp, LIB)
-    return LIB
+            raise RuntimeError(f"link of {os.path.basename(lib)} failed:\n{r.stdout}\n{r.stderr}")
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -116,10 +116,15 @@ _SIGNATURES = {
 
 
 def device_error() -> int:
-    """Read and clear the library's device error word (0 = no kernel gave up a wait)."""
+    """Read and clear the library's device error words: 0 = none; bit 0 / bit 1: a
+    prefill-attention / vertical-slash-estimate CTA gave up a wait; bit 2 (checked
+    build): a kernel met out-of-range device-side input."""
     lib = load()
     c = _c_int()
-    _check("dsa_device_error", lib.dsa_device_error(ctypes.byref(c)))
+    st = lib.dsa_device_error(ctypes.byref(c))
+    if st == -6:   # DSA_ERR_DEVICE_CHECK: the code says what was met
+        return c.value
+    _check("dsa_device_error", st)
     return c.value
 
 
@@ -144,19 +149,23 @@ def profile_collect() -> dict:
 
 
 def library_path() -> str:
-    return _build.LIB
+    """Path of the library this process loads (the checked build with DSA_CHECKED=1)."""
+    return _build.LIB_CHECKED if os.environ.get("DSA_CHECKED") == "1" else _build.LIB
 
 
 def load(build_if_missing: bool = False):
-    """Load libdsa.so (building it first if asked and absent)."""
+    """Load libdsa.so (building it first if asked and absent).  With DSA_CHECKED=1 in
+    the environment at the first call, the checked build libdsa_checked.so instead (the
+    same kernels with device-side input checks compiled in)."""
     global _lib
     if _lib is not None:
         return _lib
-    path = _build.LIB
+    checked = os.environ.get("DSA_CHECKED") == "1"
+    path = _build.LIB_CHECKED if checked else _build.LIB
     if not os.path.exists(path):
         if not build_if_missing:
-            raise ImportError(f"libdsa.so not built ({path}); run __graft_entry__.build()")
-        _build.build()
+            raise ImportError(f"{os.path.basename(path)} not built ({path}); run __graft_entry__.build()")
+        _build.build(checked=checked)
     lib = ctypes.CDLL(path)
     for name, (res, args) in _SIGNATURES.items():
         fn = getattr(lib, name, None)

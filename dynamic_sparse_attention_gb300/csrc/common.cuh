@@ -4,6 +4,36 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+// Checked builds (-DDSA_CHECKS=1): a kernel that meets device-side input outside its
+// documented range (a length, a count, a selected position, a list entry) still skips
+// or clamps it as the normal build does, and also records the fact in a check word of
+// its translation unit; dsa_device_error reports any of them as DSA_ERR_DEVICE_CHECK.
+// DSA_CHECK_WORD(name) defines the word and a host reader `int name()` (read and
+// clear; -1 on a CUDA error; always 0 in normal builds).
+#ifndef DSA_CHECKS
+#define DSA_CHECKS 0
+#endif
+#if DSA_CHECKS
+#define DSA_CHECK(cond)                                  \
+  do {                                                   \
+    if (!(cond)) atomicOr(&g_dsa_check_word, 1);         \
+  } while (0)
+#define DSA_CHECK_WORD(name)                                                         \
+  static __device__ int g_dsa_check_word;                                           \
+  int name() {                                                                       \
+    int v = 0, z = 0;                                                                \
+    if (cudaMemcpyFromSymbol(&v, g_dsa_check_word, sizeof(int)) != cudaSuccess) return -1; \
+    if (cudaMemcpyToSymbol(g_dsa_check_word, &z, sizeof(int)) != cudaSuccess) return -1;   \
+    return v;                                                                        \
+  }
+#else
+#define DSA_CHECK(cond) \
+  do {                  \
+  } while (0)
+#define DSA_CHECK_WORD(name) \
+  int name() { return 0; }
+#endif
+
 namespace dsa {
 
 constexpr unsigned kFull = 0xffffffffu;

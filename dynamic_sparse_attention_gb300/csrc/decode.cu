@@ -26,6 +26,9 @@
 #include "profile.h"
 
 namespace dsa {
+
+DSA_CHECK_WORD(decode_check_word)
+
 namespace {
 
 constexpr int kNT = 128;     // threads per split CTA
@@ -83,9 +86,12 @@ __global__ void __launch_bounds__(kNT) decode_splitk_kernel(DecodeArgs a) {
   grid_dep_wait();
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const int Tb = min(max(a.kv_len[b], 0), a.T_max);
+  const int kv_raw = a.kv_len[b], cnt_raw = a.sel_cnt[b];
+  DSA_CHECK(kv_raw >= 0 && kv_raw <= a.T_max);
+  DSA_CHECK(cnt_raw >= 0 && cnt_raw <= a.max_sel);
+  const int Tb = min(max(kv_raw, 0), a.T_max);
   const int n_s = min(a.n_sink, Tb);
-  const int cnt = min(max(a.sel_cnt[b], 0), a.max_sel);
+  const int cnt = min(max(cnt_raw, 0), a.max_sel);
   const int w0 = max(a.n_sink, Tb - a.n_stream);
   const int n_w = max(0, Tb - w0);
   const int a_len = n_s + cnt + n_w;
@@ -126,7 +132,10 @@ __global__ void __launch_bounds__(kNT) decode_splitk_kernel(DecodeArgs a) {
       int pos = -1;
       if (x < k_end) {
         if (x < n_s) pos = x;
-        else if (x < n_s + cnt) pos = sel[x - n_s];
+        else if (x < n_s + cnt) {
+          pos = sel[x - n_s];
+          DSA_CHECK(pos >= a.n_sink && pos < max(a.n_sink, Tb - a.n_stream));
+        }
         else pos = w0 + (x - n_s - cnt);
         if (pos < 0 || pos >= Tb) pos = -1;   // never read outside the row's context
       }

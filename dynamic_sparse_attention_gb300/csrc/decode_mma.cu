@@ -54,6 +54,9 @@
 #include "profile.h"
 
 namespace dsa {
+
+DSA_CHECK_WORD(decode_mma_check_word)
+
 namespace {
 
 // Ring slots: a bf16 sub-tile (K and V rows of 16 keys) is 8 KiB at d = 128, an FP8 one
@@ -139,7 +142,9 @@ __global__ void __launch_bounds__(NW * 32) decode_mma_kernel(DecodeArgs a) {
   // slots [rank * sel_per, +sel_per).  The fixed keys are gathered and scored before
   // the wait on the previous kernel (the selection's last kernel, which writes
   // sel_idx / sel_cnt and lets this grid start early); only the selected ones after it.
-  const int Tb = min(max(a.kv_len[b], 0), a.T_max);
+  const int kv_raw = a.kv_len[b];
+  DSA_CHECK(kv_raw >= 0 && kv_raw <= a.T_max);
+  const int Tb = min(max(kv_raw, 0), a.T_max);
   const int n_s = min(a.n_sink, Tb);
   const int w0 = max(a.n_sink, Tb - a.n_stream);
   const int n_w = max(0, Tb - w0);
@@ -351,13 +356,16 @@ __global__ void __launch_bounds__(NW * 32) decode_mma_kernel(DecodeArgs a) {
 
   grid_dep_wait();
   const int32_t *sel = a.sel_idx + static_cast<size_t>(b) * a.max_sel;
-  const int cnt = min(max(a.sel_cnt[b], 0), a.max_sel);
+  const int cnt_raw = a.sel_cnt[b];
+  DSA_CHECK(cnt_raw >= 0 && cnt_raw <= a.max_sel);
+  const int cnt = min(max(cnt_raw, 0), a.max_sel);
   const int s_begin = rank * a.sel_per;
   const int s_end = min(cnt, s_begin + a.sel_per);
   const int ns_sub = s_end > s_begin ? (s_end - s_begin + kST - 1) / kST : 0;
   for (int i = tid; i < a.sel_per; i += kThreads) {
     const int x = s_begin + i;
     int pos = x < s_end ? __ldg(sel + x) : -1;
+    DSA_CHECK(x >= s_end || (pos >= a.n_sink && pos < max(a.n_sink, Tb - a.n_stream)));
     s_poss[i] = (pos >= 0 && pos < Tb) ? pos : -1;   // never read outside the row's context
   }
   __syncthreads();

@@ -30,6 +30,9 @@
 #include "mma_sync.cuh"
 
 namespace dsa {
+
+DSA_CHECK_WORD(hip_select_check_word)
+
 namespace {
 
 struct InputRange {
@@ -44,13 +47,17 @@ __device__ __forceinline__ InputRange stage_input(const int32_t *kv_len, int b, 
                                                   int in_stride) {
   InputRange r;
   if (in_idx == nullptr) {
-    const int Tb = min(max(kv_len[b], 0), T_max);
+    const int kv_raw = kv_len[b];
+    DSA_CHECK(kv_raw >= 0 && kv_raw <= T_max);
+    const int Tb = min(max(kv_raw, 0), T_max);
     r.start = n_sink;
     r.n_in = max(0, Tb - n_stream - n_sink);
     r.in = nullptr;
   } else {
+    const int cnt_raw = in_cnt[b];
+    DSA_CHECK(cnt_raw >= 0 && cnt_raw <= in_stride);
     r.start = 0;
-    r.n_in = min(max(in_cnt[b], 0), in_stride);
+    r.n_in = min(max(cnt_raw, 0), in_stride);
     r.in = in_idx + static_cast<size_t>(b) * in_stride;
   }
   return r;
@@ -144,8 +151,11 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
   const TQ *q = static_cast<const TQ *>(a.q) + static_cast<size_t>(b) * a.T_q * a.H_q * D;
   if (!ROWS && ir.in) {
     const int len0 = min(a.L, ir.n_in - j0 * a.L);
-    for (int x = threadIdx.x; x < len0; x += blockDim.x)
-      s_pos[x] = min(max(x == static_cast<int>(threadIdx.x) ? pv : ir.in[j0 * a.L + x], 0), a.T_max - 1);
+    for (int x = threadIdx.x; x < len0; x += blockDim.x) {
+      const int raw = x == static_cast<int>(threadIdx.x) ? pv : ir.in[j0 * a.L + x];
+      DSA_CHECK(raw >= 0 && raw < a.T_max);   // a list entry (cached lists: as stored)
+      s_pos[x] = min(max(raw, 0), a.T_max - 1);
+    }
   }
   if (!QREG) {
     const int n = a.T_q * a.H_q * D;

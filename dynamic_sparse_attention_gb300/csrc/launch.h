@@ -172,6 +172,12 @@ cudaError_t launch_vs_tc(const VsTcLaunch &l, cudaStream_t s);
 int vs_tc_device_error();        // the estimate's device error word (read and cleared)
 // wait limits of the tensor-core kernels' bounded waits (0 on success)
 int vs_tc_set_wait_limit(unsigned long long ns);
+// check words of a checked build (DSA_CHECKS; read and cleared; 0 in normal builds)
+int decode_check_word();
+int decode_mma_check_word();
+int hip_select_check_word();
+int stage_tc_check_word();
+int prefill_tc_check_word();
 int prefill_tc_set_wait_limit(unsigned long long ns);
 
 // Sparse prefill attention over tile / column lists.

@@ -58,6 +58,9 @@
 #include "tc_ptx.cuh"
 
 namespace dsa {
+
+DSA_CHECK_WORD(prefill_tc_check_word)
+
 namespace {
 
 using namespace tc;
@@ -259,17 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   // tile lists -> bitmaps; a block after a half's own query block is fully masked there
   {
-    const int c = min(max(a.blk_cnt[bh * a.n_qblk + m0], 0), a.max_blk);
+    const int c_raw = a.blk_cnt[bh * a.n_qblk + m0];
+    DSA_CHECK(c_raw >= 0 && c_raw <= a.max_blk);
+    const int c = min(max(c_raw, 0), a.max_blk);
     const int32_t *l0 = a.blk_idx + (bh * a.n_qblk + m0) * static_cast<size_t>(a.max_blk);
     for (int i = tid; i < c; i += kThreads) {
       const int n = l0[i];
+      DSA_CHECK(n >= 0 && n < a.n_qblk);
       if (n >= 0 && n <= m0) atomicOr(&bm0[n >> 5], 1u << (n & 31));
     }
     if (has1) {
-      const int c1 = min(max(a.blk_cnt[bh * a.n_qblk + m1], 0), a.max_blk);
+      const int c1_raw = a.blk_cnt[bh * a.n_qblk + m1];
+      DSA_CHECK(c1_raw >= 0 && c1_raw <= a.max_blk);
+      const int c1 = min(max(c1_raw, 0), a.max_blk);
       const int32_t *l1 = a.blk_idx + (bh * a.n_qblk + m1) * static_cast<size_t>(a.max_blk);
       for (int i = tid; i < c1; i += kThreads) {
         const int n = l1[i];
+        DSA_CHECK(n >= 0 && n < a.n_qblk);
         if (n >= 0 && n <= m1) atomicOr(&bm1[n >> 5], 1u << (n & 31));
       }
     }
@@ -286,8 +295,11 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const int n_blk_t = (*n_blk_tiles_s + 1) / 2;   // listed blocks, two per tile
-  const int c0 = min(max(a.col_cnt[bh * a.n_qblk + m0], 0), a.max_col);
-  const int c1 = has1 ? min(max(a.col_cnt[bh * a.n_qblk + m1], 0), a.max_col) : 0;
+  const int cc0_raw = a.col_cnt[bh * a.n_qblk + m0];
+  const int cc1_raw = has1 ? a.col_cnt[bh * a.n_qblk + m1] : 0;
+  DSA_CHECK(cc0_raw >= 0 && cc0_raw <= a.max_col && cc1_raw >= 0 && cc1_raw <= a.max_col);
+  const int c0 = min(max(cc0_raw, 0), a.max_col);
+  const int c1 = has1 ? min(max(cc1_raw, 0), a.max_col) : 0;
   const int nct0 = (c0 + kKeys - 1) / kKeys, nct1 = (c1 + kKeys - 1) / kKeys;
   const int T = n_blk_t + nct0 + nct1;
   const uint32_t tmem = *tmem_slot;
@@ -349,6 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         for (int i = 0; i < kKeys / 32; ++i) {
           const int x = lane + 32 * i;
           int j = x < ncol ? cl[cb + x] : -1;
+          DSA_CHECK(x >= ncol || (j >= 0 && j < a.S));
           if (j < 0 || j > last_row) j = -1;
           pos[i] = j;
         }
@@ -764,7 +777,18 @@ extern "C" int dsa_device_error(int *code) {
   if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
   const int w = vs_tc_device_error();   // the vertical-slash estimate's word
   if (w < 0) return fail(DSA_ERR_CUDA, "reading the estimate's device error word");
-  *code = v | (w << 1);
+  // checked builds: out-of-range device-side inputs met by the kernels
+  int chk = 0;
+  const int words[5] = {decode_check_word(), decode_mma_check_word(), hip_select_check_word(),
+                        stage_tc_check_word(), prefill_tc_check_word()};
+  for (int x : words) {
+    if (x < 0) return fail(DSA_ERR_CUDA, "reading a device check word");
+    chk |= x;
+  }
+  *code = v | (w << 1) | (chk ? 4 : 0);
+  if (chk)
+    return fail(DSA_ERR_DEVICE_CHECK, "a kernel met a device-side input outside its range "
+                                      "(length, count, selected position or list entry)");
   return DSA_OK;
 }
 

@@ -34,6 +34,9 @@
 #include "mma_sync.cuh"
 
 namespace dsa {
+
+DSA_CHECK_WORD(stage_tc_check_word)
+
 namespace {
 
 constexpr int kTcMaxListSmem = 32 * 1024;   // bytes of staged list positions per CTA
@@ -79,15 +82,27 @@ __global__ void __launch_bounds__(256, 4) stage_score_tc_kernel(StageScoreArgs a
   }
   int n_in, start;
   if (lst) {
-    n_in = min(max(a.in_cnt[b], 0), a.in_stride);
+    const int cnt_raw = a.in_cnt[b];
+    DSA_CHECK(cnt_raw >= 0 && cnt_raw <= a.in_stride);
+    n_in = min(max(cnt_raw, 0), a.in_stride);
     start = 0;
   } else {
-    const int Tb = min(max(a.kv_len[b], 0), a.T_max);
+    const int kv_raw = a.kv_len[b];
+    DSA_CHECK(kv_raw >= 0 && kv_raw <= a.T_max);
+    const int Tb = min(max(kv_raw, 0), a.T_max);
     n_in = max(0, Tb - a.n_stream - a.n_sink);
     start = a.n_sink;
   }
   const int n_chunk = (n_in + a.L - 1) / a.L;
   if (j0 >= n_chunk) return;   // nothing in flight yet that outlives the CTA
+#if DSA_CHECKS
+  if (lst)   // the list entries this CTA uses (cached lists: as stored)
+    for (int x = threadIdx.x; x < CPW * a.L; x += blockDim.x)
+      if (j0 * a.L + x < n_in) {
+        const int raw = __ldg(lst + j0 * a.L + x);
+        DSA_CHECK(raw >= 0 && raw < a.T_max);
+      }
+#endif
   __syncthreads();             // staged positions
 
   auto pos_of = [&](int c, int x) -> int {

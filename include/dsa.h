@@ -32,8 +32,11 @@
  *     nothing is launched and no output is touched; dsa_last_error() gives a
  *     message (thread-local).  DSA_ERR_CUDA reports a launch failure.
  *   - Device-side data (kv_len, counts, index lists) is not read by the host.
- *     Out-of-range values are clamped in the kernels (kv_len to [0, T_max],
- *     counts to [0, capacity]); index entries must be valid positions.
+ *     Out-of-range values are clamped or skipped in the kernels (kv_len to
+ *     [0, T_max], counts to [0, capacity], positions outside the row or the
+ *     sequence skipped), never dereferenced.  A checked build (compiled with
+ *     -DDSA_CHECKS=1, libdsa_checked.so) also records every such value it meets
+ *     and dsa_device_error then returns DSA_ERR_DEVICE_CHECK.
  */
 #ifndef DSA_H_
 #define DSA_H_
@@ -55,7 +58,7 @@ typedef enum {
   DSA_ERR_WORKSPACE = -3,    /* ws missing or ws_bytes below the *_workspace() size */
   DSA_ERR_ALIGNMENT = -4,    /* a pointer is NULL or misaligned */
   DSA_ERR_CUDA = -5,         /* a kernel launch failed (message from the CUDA runtime) */
-  DSA_ERR_DEVICE_CHECK = -6  /* reserved for device-side checks */
+  DSA_ERR_DEVICE_CHECK = -6  /* checked builds: a kernel met out-of-range device data */
 } dsa_status;
 
 /* Element types of q / k / v (out has the type of q):
@@ -421,7 +424,9 @@ int dsa_profile_collect(dsa_kernel_stat *out, int max_out, int *n_out);
  * of the vertical-slash estimate) is bounded; a CTA that gives up stops issuing work,
  * frees its resources and sets a device error word (the prefill CTA also writes zero
  * output).  dsa_device_error copies the words to *code (0 = none; bit 0: the prefill
- * attention, bit 1: the estimate) and clears them.  It synchronises with the device
+ * attention, bit 1: the estimate; bit 2: in a checked build, a kernel met a kv_len,
+ * count, selected position or list entry outside its documented range -- the call then
+ * returns DSA_ERR_DEVICE_CHECK) and clears them.  It synchronises with the device
  * (cudaMemcpyFromSymbol); call it between steps, not on a hot path.  Not a
  * source-page operation. */
 int dsa_device_error(int *code);
