@@ -143,7 +143,9 @@ def test_block_sparse_128k_config():
     out, lse = dsa.sparse_attn_prefill(q, k, v, idx["blk_cnt"], idx["blk_idx"], idx["col_cnt"], None)
     torch.cuda.synchronize()
     nq = 2048
-    heads, rows = (0, 13, 31), (0, 1, 99, 100, 777, 1500, nq - 1)
+    # 64 rows spread over the sequence (the first and last among them) for three heads
+    heads = (0, 13, 31)
+    rows = sorted(set([0, 1, 99, 100] + np.linspace(0, nq - 1, 64).astype(int).tolist()))
     qp = idx["q_pool"].cpu().numpy()
     sc = idx["scores"].cpu().numpy()
     for h in heads:
@@ -159,7 +161,10 @@ def test_block_sparse_128k_config():
             s32 = sc[0, h, m, :m + 1]
             assert np.all(np.abs(s32 - z) <= 1e-5 * np.abs(z).max() + 1e-6)
             check_topk_list(s32, A, min(100, m + 1), _lists(idx, 0, h, m), floor=1e-9)
-    _check_attention(c, idx, out, lse, [(0, h, m) for h in heads for m in (0, 100, 1500, nq - 1)])
+    # attention: the same rows for the three heads, the first and last block of every head
+    pairs = [(0, h, m) for h in heads for m in rows]
+    pairs += [(0, h, m) for h in range(c.H_q) if h not in heads for m in (0, nq - 1)]
+    _check_attention(c, idx, out, lse, pairs)
 
 
 def test_ashape_128k_config():

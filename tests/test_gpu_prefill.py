@@ -179,9 +179,13 @@ def test_prefill_128k_config():
                                        idx["col_idx"])
     torch.cuda.synchronize()
     nq = c.S // 64
-    blocks = [0, 1, 2, 63, 64, 500, 1023, 1500, nq - 2, nq - 1]
+    # 64 query blocks spread over the sequence (the first and last among them) for three
+    # heads, and the first and last blocks of every head
+    blocks = sorted(set(np.linspace(0, nq - 1, 64).astype(int).tolist()))
     _check_index(c, idx, heads=[0, 13, 31], blocks=blocks)
-    pairs = [(0, h, m) for h in (0, 13, 31) for m in (0, 1, 777, nq - 1)]
+    _check_index(c, idx, heads=[h for h in range(c.H_q) if h not in (0, 13, 31)], blocks=[0, nq - 1])
+    pairs = [(0, h, m) for h in (0, 13, 31) for m in blocks]
+    pairs += [(0, h, m) for h in range(c.H_q) if h not in (0, 13, 31) for m in (0, nq - 1)]
     _check_attention(c, idx, out, lse, pairs)
     # planted structure shows up in the estimate (generator self-check, not parity)
     vert = idx["vertical"].cpu().numpy()[0]
