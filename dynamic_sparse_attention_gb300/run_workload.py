@@ -8,6 +8,8 @@ Workloads (seeded generators of the `synth` module at the repository root):
   decode_128k  the same at context 131,072
   prefill_128k vs_index_build + sparse_attn_prefill, S=131072, 32/8 heads, d=128
   prefill_16k  the same at S=16384
+  prefill_128k_h4  the same at S=131072 with 4 query heads / 1 KV head (the per-CTA tile
+               counts of the 128K workload in about 0.3 GB of device memory)
   prefill_bs_32k  block_sparse_index_build (k_b=100) + sparse_attn_prefill at S=32768
   prefill_hip_16k  hip_prefill_select + hip_prefill_lists + sparse_attn_prefill at S=16384
                    (chunks 256 / 32 / 8, keep 4096 / 2048 / 1024, sink 256, window 1024)
@@ -81,7 +83,7 @@ def _prefill_hip(case, iters, cfg):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("workload", choices=["decode_1m", "decode_128k", "prefill_128k", "prefill_16k",
-                                        "prefill_bs_32k", "prefill_hip_16k"])
+                                        "prefill_128k_h4", "prefill_bs_32k", "prefill_hip_16k"])
     p.add_argument("--iters", type=int, default=4)
     args = p.parse_args(argv)
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -95,6 +97,9 @@ def main(argv=None):
         _decode(synth.decode_128k(), args.iters)
     elif args.workload == "prefill_128k":
         _prefill(synth.prefill_128k(), args.iters)
+    elif args.workload == "prefill_128k_h4":
+        _prefill(synth.prefill_case("prefill_vs_S131072_h4", S=131072, H_q=4, H_kv=1, D=128, seed=4),
+                 args.iters)
     elif args.workload == "prefill_hip_16k":
         _prefill_hip(synth.prefill_case("prefill_hip_S16384", S=16384, H_q=32, H_kv=8, D=128, seed=4),
                      args.iters, dsa.HipConfig((256, 32, 8), (4096, 2048, 1024), 256, 1024))
