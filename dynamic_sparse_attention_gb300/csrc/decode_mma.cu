@@ -576,10 +576,10 @@ cudaError_t launch_mma_d(const DecodeArgs &a0, cudaStream_t s) {
     return e;
   };
   // Candidates, best first.  Eight warps with two ring slots consume a 1M-context
-  // range's selected sub-tiles in one round, but at about 100 registers a thread two
-  // such CTAs fit an SM where three four-warp CTAs do: they are taken only when every
-  // cluster of the launch fits the GPU at once.  Otherwise four warps (the deepest ring
-  // first); clusters of 8 where 16-CTA clusters cannot be co-scheduled at all.
+  // range's selected sub-tiles in one round, but their 128 KB of ring (like four warps
+  // with four slots) leaves one CTA per SM: they are taken only when every cluster of
+  // the launch fits the GPU at once.  Otherwise four warps with three slots (two CTAs
+  // per SM); clusters of 8 where 16-CTA clusters cannot be co-scheduled at all.
   const int C0 = a.n_split;
   MmaShape cands[5];
   int n_c = 0;
