@@ -89,6 +89,12 @@ __device__ __forceinline__ void cp_async_16(void *smem_dst, const void *gmem_src
                "l"(gmem_src));
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::); }
+// The mbarrier tracks this thread's earlier cp.async copies: its pending count goes up
+// by one now and down by one once they have all landed (no effect on the arrival count
+// the barrier expects).
+__device__ __forceinline__ void cp_async_mbar_arrive(uint64_t *bar) {
+  asm volatile("cp.async.mbarrier.arrive.shared::cta.b64 [%0];\n" ::"r"(smem_addr(bar)) : "memory");
+}
 template <int N>
 __device__ __forceinline__ void cp_async_wait() {
   asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");

@@ -18,9 +18,10 @@
 // and keys past the sequence end.
 // Warp roles (352 threads):
 //   warp 0     K producer: Q once (TMA), then K tiles (two 64-row TMA boxes per 64-wide
-//              head-dim half for block tiles, 16-byte cp.async gathers for column tiles)
-//              into a 3-stage ring; writes each tile's description (kind, the block of
-//              each half, per-half membership, column positions);
+//              head-dim half for block tiles, 16-byte cp.async gathers for column tiles,
+//              which complete on the stage's mbarrier while the warp moves on) into a
+//              3-stage ring; writes each tile's description (kind, the block of each
+//              half, per-half membership, column positions);
 //   warp 1     V producer: V tiles into a 2-stage ring (its own walk of the same lists);
 //   warp 2     MMA issuer (one thread): S_b = Q K^T (M = N = 128, K = D) into one of three
 //              TMEM score buffers (b = tile mod 3), O += P V (A = P read from TMEM,
@@ -29,13 +30,15 @@
 //   warps 3-10 softmax: two threads per query row; warp w reads the TMEM lanes of
 //              quarter w % 4 and the 64-key half w / 4 of the tile.  The two halves of a
 //              row exchange their maxima through shared memory (an mbarrier per lane
-//              quarter); each thread then forms P = exp2(s * scale * log2e - max) with
-//              the exact running max (the row's largest probability is exactly 1, free
-//              of bf16 rounding), keeps a partial row sum, and writes its bf16 pairs over
-//              the first 64 columns of S_b, where the P V MMA reads them, while the next
-//              tile's scores stream in from TMEM.  When the max grows, each warp brings
-//              its quarter of O to the new max once P V of the previous tile has
-//              retired.  The epilogue adds the partial sums, normalises and stores.
+//              quarter); each thread then forms P = exp2(s * scale * log2e - m) against
+//              a reference m that follows the running max lazily: it moves to the max
+//              only once the max exceeds it by more than kRescaleSlack (so P <= 2),
+//              keeps a partial row sum, and writes its bf16 pairs over the first 64
+//              columns of S_b, where the P V MMA reads them, while the next tile's scores
+//              stream in from TMEM.  When the reference moves, each warp brings its
+//              quarter of O to it once P V of the previous tile has retired (a wait that
+//              drains the MMA pipe, hence the slack).  The epilogue adds the partial
+//              sums, normalises and stores.
 // Operands: Q and K tiles are K-major with 128-byte swizzle (what TMA writes for a
 // 64-element-wide box); V tiles are the B operand in MN-major form (keys along K).
 // Every mbarrier wait is bounded; on a timeout the CTA stops issuing work, drains its
@@ -79,6 +82,12 @@ constexpr int kThreads = (3 + kSmWarps) * 32;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+// log2 units by which a row's max may exceed its softmax reference before the
+// reference (and O with it) is moved.  With 1, P <= 2 and the bf16 rounding of the
+// probabilities is that of the exact-max form (measured on the parity cases: the same
+// worst error; 2 and 4 raise it, 4 past the 1e-2 bound), while most of the rescales,
+// each a wait on the previous P V by every warp with a row whose max moved, go away.
+constexpr float kRescaleSlack = 1.f;
 
 static __device__ int g_prefill_tc_error;   // sticky error word, read by dsa_device_error
 static __device__ int g_abort_epoch;         // launch epoch of a launch in which a CTA gave up
@@ -90,6 +99,9 @@ struct TileMeta {
   int kind;          // 0: block tile (two 64-key list blocks), 1: gathered column tile
   int mask;          // bit 2*grp + half: rows of query block m_grp use that 64-key half
   int blk[2];        // the 64-key block held by each half (kind 0)
+  int below;         // kind 1: every key precedes every row of the tile's query block
+  int pad[3];
+  uint32_t nonempty[kKeys / 32];   // kind 1: bit x: slot x holds a key
   int pos[kKeys];    // key positions of a column tile (-1: empty slot)
 };
 static_assert(sizeof(TileMeta) % 16 == 0 && offsetof(TileMeta, pos) % 16 == 0, "int4 reads of pos");
@@ -232,10 +244,14 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   const WaitCtx wc{abort_flag, a.epoch};
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // longest rows first; the G query heads of one KV head side by side, so the CTAs that
+  // read the same key and value rows (for lists shared by the heads, the same rows)
+  // run together and share them through L2
   const int n_pairs = (a.n_qblk + 1) / 2;
-  const int p = n_pairs - 1 - static_cast<int>(blockIdx.x);   // longest rows first
-  const int h = blockIdx.y, b = blockIdx.z;
-  const int g = h / (a.H_q / a.H_kv);
+  const int G = a.H_q / a.H_kv;
+  const int p = n_pairs - 1 - static_cast<int>(blockIdx.x) / G;
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int h = g * G + static_cast<int>(blockIdx.x) % G;
   const int m0 = 2 * p, m1 = 2 * p + 1;
   const bool has1 = m1 < a.n_qblk;
   const size_t bh = static_cast<size_t>(b) * a.H_q + h;
@@ -367,29 +383,43 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         }
         if (is_k) {
           TileMeta *md = &meta[t % kMetaRing];
+          bool below = true;   // no key after the first row of block mg: no causal masking
 #pragma unroll
-          for (int i = 0; i < kKeys / 32; ++i) md->pos[lane + 32 * i] = pos[i];
+          for (int i = 0; i < kKeys / 32; ++i) {
+            md->pos[lane + 32 * i] = pos[i];
+            const uint32_t ne = __ballot_sync(kFull, pos[i] >= 0);
+            if (lane == 0) md->nonempty[i] = ne;
+            below = below && pos[i] <= kBlk * mg;
+          }
+          below = __all_sync(kFull, below);
           if (lane == 0) {
             md->kind = 1;
             md->mask = grp == 0 ? 0x3 : 0xC;
             md->blk[0] = md->blk[1] = -1;
+            md->below = below ? 1 : 0;
           }
         }
-        // key row x = lane + 32 i; 16-byte chunk c lies in dims half c >> 3, swizzled in its row
-#pragma unroll 1
-        for (int c = 0; c < D / 8; ++c) {
-          const int hh = c >> 3, cc = c & 7;
+        // Eight lanes per key row, one 16-byte chunk cc of a 64-dim half each, so one
+        // instruction of the warp copies four whole 128-byte row segments (rows 4r ..
+        // 4r + 3; row x's position is held by lane x % 32 in pos[x / 32]); chunk cc of
+        // row x lands at chunk cc ^ (x & 7) of its swizzled 128-byte row.
+        const int sub = lane >> 3, cc = lane & 7;
 #pragma unroll
-          for (int i = 0; i < kKeys / 32; ++i) {
-            const int x = lane + 32 * i;
+        for (int r = 0; r < kKeys / 4; ++r) {
+          const int x = 4 * r + sub;
+          const int j = __shfl_sync(kFull, pos[r >> 3], x & 31);
+          const uint16_t *row = src + static_cast<size_t>(j) * krow + cc * 8;
+#pragma unroll
+          for (int hh = 0; hh < L::kHalves; ++hh) {
             unsigned char *dst = stage + hh * L::kHalf + x * 128 + ((cc ^ (x & 7)) << 4);
-            if (pos[i] >= 0) cp_async_16(dst, src + static_cast<size_t>(pos[i]) * krow + c * 8);
+            if (j >= 0) cp_async_16(dst, row + 64 * hh);
             else *reinterpret_cast<uint4 *>(dst) = make_uint4(0, 0, 0, 0);
           }
         }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
+        // the stage completes once every lane's copies have landed; the producer goes on
+        // to the next tile meanwhile (the consumer orders them for the tensor core)
+        fence_proxy_async_smem();   // the zero fills
+        cp_async_mbar_arrive(&full[st]);
         __syncwarp();
         if (lane == 0) mbar_arrive(&full[st]);
       }
@@ -413,6 +443,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int st = t % kKS;
         if (!tc_wait(&k_full[st], (t / kKS) & 1, wc)) return false;
         tc_fence_after();
+        fence_proxy_async_smem();   // gathered rows were written by cp.async (generic proxy)
         const uint32_t d = tmem + static_cast<uint32_t>((t % kSB) * kKeys);
         const uint32_t kbase = sK + st * L::kTile;
 #pragma unroll
@@ -429,6 +460,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int st = t % kVS;
         if (!tc_wait(&v_full[st], (t / kVS) & 1, wc)) return false;
         tc_fence_after();
+        fence_proxy_async_smem();
         const uint32_t vbase = sV + st * L::kTile;
         const uint32_t pcol = tmem + static_cast<uint32_t>((t % kSB) * kKeys);
 #pragma unroll
@@ -472,10 +504,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const float sl2 = a.sl2;
     const float2 sl2x2 = make_float2(sl2, sl2);
     const int last_key = min(qpos, a.S - 1);   // causal and in-sequence bound of the row
-    float m_cur = -INFINITY, l = 0.f;   // running max (base-2 units), this slice's row sum
+    float m_cur = -INFINITY, l = 0.f;   // softmax reference (base-2 units), this slice's row sum
     float m_o = -INFINITY;              // max that O is currently relative to
     bool ok = true;
     uint32_t sc[kSW];                   // this slice's scores (then those of the next tile)
+    bool slice_dead = false;            // no key of the last published tile's slice is in
+                                        // any row of this warp (warp-uniform)
 
     // TMEM column of 32-column part i of this slice in score buffer t % 3
     auto s_addr = [&](int t, int i) {
@@ -486,48 +520,73 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
       const TileMeta *md = &meta[t % kMetaRing];
       const int kind = md->kind;
       const int hmask = row_ok ? (md->mask >> (2 * grp)) & 3 : 0;   // halves this row uses
-      uint32_t valid = 0u;   // bit c: slot c of a 32-slot part is a key of the row
       int lim = 0;
+      bool below = false;
       if (kind == 0) {
         // slice cs is 64-key half cs, whose slot c holds key 64 * blk[cs] + c
         static_assert(kSW == kBlk, "one softmax slice per 64-key half");
         const bool member = (hmask >> cs) & 1;
         lim = member ? last_key - kBlk * md->blk[cs] : -1;   // slots <= lim are keys
+      } else {
+        below = md->below != 0;
       }
       tmem_wait_ld();
       const bool trim = kind != 0 || lim < kSW - 1;
+      bool dead = false;
       if (__any_sync(kFull, trim)) {
-#pragma unroll 1
+        uint32_t valid[kSW / 32];   // bit c: slot c of 32-slot part i is a key of the row
+#pragma unroll
         for (int i = 0; i < kSW / 32; ++i) {
           if (kind == 0) {
             const int li = lim - 32 * i;
-            valid = li < 0 ? 0u : (li >= 31 ? 0xffffffffu : (2u << li) - 1u);
+            valid[i] = li < 0 ? 0u : (li >= 31 ? 0xffffffffu : (2u << li) - 1u);
+          } else if (hmask == 0) {
+            valid[i] = 0u;   // the tile belongs to the other query block
+          } else if (below) {
+            valid[i] = md->nonempty[(kSW * cs) / 32 + i];
           } else {
-            valid = 0u;
+            uint32_t v = 0u;
             const int4 *pp = reinterpret_cast<const int4 *>(md->pos + kSW * cs + 32 * i);
 #pragma unroll 1
             for (int c4 = 0; c4 < 8; ++c4) {
               const int4 j = pp[c4];
-              valid |= (static_cast<uint32_t>(j.x >= 0 && j.x <= qpos) << (4 * c4)) |
-                       (static_cast<uint32_t>(j.y >= 0 && j.y <= qpos) << (4 * c4 + 1)) |
-                       (static_cast<uint32_t>(j.z >= 0 && j.z <= qpos) << (4 * c4 + 2)) |
-                       (static_cast<uint32_t>(j.w >= 0 && j.w <= qpos) << (4 * c4 + 3));
+              v |= (static_cast<uint32_t>(j.x >= 0 && j.x <= qpos) << (4 * c4)) |
+                   (static_cast<uint32_t>(j.y >= 0 && j.y <= qpos) << (4 * c4 + 1)) |
+                   (static_cast<uint32_t>(j.z >= 0 && j.z <= qpos) << (4 * c4 + 2)) |
+                   (static_cast<uint32_t>(j.w >= 0 && j.w <= qpos) << (4 * c4 + 3));
             }
-            if (hmask == 0) valid = 0u;
+            valid[i] = v;
           }
+        }
+        uint32_t any = 0u;
 #pragma unroll
-          for (int c = 0; c < 32; ++c)
-            if (i == 0) sc[c] = (valid >> c) & 1u ? sc[c] : __float_as_uint(-INFINITY);
-            else if (kSW > 32) sc[32 + c] = (valid >> c) & 1u ? sc[32 + c] : __float_as_uint(-INFINITY);
+        for (int i = 0; i < kSW / 32; ++i) any |= valid[i];
+        // a slice no row of the warp uses (the other query block's column tile, or a
+        // 64-key block only the other block lists) needs neither masking nor exponentials
+        dead = __all_sync(kFull, any == 0u);
+        if (!dead) {
+#pragma unroll
+          for (int i = 0; i < kSW / 32; ++i) {
+            if (__any_sync(kFull, valid[i] != 0xffffffffu)) {
+#pragma unroll
+              for (int c = 0; c < 32; ++c)
+                sc[32 * i + c] = (valid[i] >> c) & 1u ? sc[32 * i + c] : __float_as_uint(-INFINITY);
+            }
+          }
         }
       }
-      float mx[4];
+      float m = -INFINITY;
+      if (!dead) {
+        float mx[4];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
+        for (int i = 0; i < 4; ++i) mx[i] = -INFINITY;
 #pragma unroll
-      for (int c = 0; c < kSW; c += 2)
-        mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sc[c]), __uint_as_float(sc[c + 1]));
-      red[((t & 1) * kSlices + cs) * kRowsQ + row] = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+        for (int c = 0; c < kSW; c += 2)
+          mx[(c >> 1) & 3] = fmax3(mx[(c >> 1) & 3], __uint_as_float(sc[c]), __uint_as_float(sc[c + 1]));
+        m = fmax3(mx[0], mx[1], fmaxf(mx[2], mx[3]));
+      }
+      slice_dead = dead;
+      red[((t & 1) * kSlices + cs) * kRowsQ + row] = m;
       __syncwarp();
       if (lane == 0) mbar_arrive(&qbar[t & 1]);
     };
@@ -535,6 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     // rescale, release of P
     auto finish_tile = [&](int t) -> bool {
       const bool more = t + 1 < T;
+      const bool dead = slice_dead;   // publish_max(t + 1) below overwrites it
       // tile t's phase on its exchange barrier is its (t / 2)-th; the warp itself waited
       // the one before, and the one after needs this warp's own arrival
       if (!warp_wait(&qbar[t & 1], (t >> 1) & 1, wc)) return false;
@@ -543,7 +603,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
       for (int i = 1; i < kSlices; ++i) mraw = fmaxf(mraw, rr[i * kRowsQ]);
       const float mt = mraw * sl2;
-      if (mt > m_cur) {   // sl2 > 0: same order as the scaled scores
+      // sl2 > 0: same order as the scaled scores; -inf + slack stays -inf
+      if (mt > m_cur + kRescaleSlack) {
         if (m_cur != -INFINITY) l *= fast_exp2(m_cur - mt);
         m_cur = mt;
       }
@@ -558,14 +619,19 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
       for (int i = 0; i < kSW / 32; ++i) {
         uint32_t pk[16];
+        if (dead) {   // every probability of the slice is 0
 #pragma unroll
-        for (int c = 0; c < 32; c += 2) {
-          const int k = 32 * i + c;
-          const float2 y = ffma2(make_float2(__uint_as_float(sc[k]), __uint_as_float(sc[k + 1])), sl2x2, nm2);
-          const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
-          if ((c >> 1) & 1) acc1 = fadd2(acc1, e);
-          else acc0 = fadd2(acc0, e);
-          pk[c >> 1] = pack_bf16x2(e.x, e.y);
+          for (int c = 0; c < 16; ++c) pk[c] = 0u;
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) {
+            const int k = 32 * i + c;
+            const float2 y = ffma2(make_float2(__uint_as_float(sc[k]), __uint_as_float(sc[k + 1])), sl2x2, nm2);
+            const float2 e = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+            if ((c >> 1) & 1) acc1 = fadd2(acc1, e);
+            else acc0 = fadd2(acc0, e);
+            pk[c >> 1] = pack_bf16x2(e.x, e.y);
+          }
         }
         tmem_st16(pcol + 16 * i, pk);
         if (more) {   // part i of this slice is free: bring in tile t + 1's
@@ -735,7 +801,7 @@ cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
   auto kern = prefill_tc_kernel<D>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  dim3 grid((a.n_qblk + 1) / 2, pa.H_q, pa.B);
+  dim3 grid((a.n_qblk + 1) / 2 * (pa.H_q / pa.H_kv), pa.H_kv, pa.B);
   {
     ProfScope ps("prefill_attention_tc", s);
     kern<<<grid, kThreads, smem, s>>>(a);

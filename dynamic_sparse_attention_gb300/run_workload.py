@@ -13,6 +13,9 @@ Workloads (seeded generators of the `synth` module at the repository root):
   prefill_bs_32k  block_sparse_index_build (k_b=100) + sparse_attn_prefill at S=32768
   prefill_hip_16k  hip_prefill_select + hip_prefill_lists + sparse_attn_prefill at S=16384
                    (chunks 256 / 32 / 8, keep 4096 / 2048 / 1024, sink 256, window 1024)
+  prefill_hip_128k_h4  the same at S=131072 with 4 query heads / 1 KV head and the 128K
+                   stage table (keep 32768 / 8192 / 2048): the per-CTA tile counts of the
+                   128K InfiniteHiP prefill in well under 1 GB of device memory
 Each iteration launches the workload's kernels once on the current stream; nothing is
 timed or checked.  The first iteration is a warm-up like any other, so a profiler
 that skips the first launches of a kernel sees steady-state ones.
@@ -83,7 +86,8 @@ def _prefill_hip(case, iters, cfg):
 def main(argv=None):
     p = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     p.add_argument("workload", choices=["decode_1m", "decode_128k", "prefill_128k", "prefill_16k",
-                                        "prefill_128k_h4", "prefill_bs_32k", "prefill_hip_16k"])
+                                        "prefill_128k_h4", "prefill_bs_32k", "prefill_hip_16k",
+                                        "prefill_hip_128k_h4"])
     p.add_argument("--iters", type=int, default=4)
     args = p.parse_args(argv)
     sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
@@ -103,6 +107,9 @@ def main(argv=None):
     elif args.workload == "prefill_hip_16k":
         _prefill_hip(synth.prefill_case("prefill_hip_S16384", S=16384, H_q=32, H_kv=8, D=128, seed=4),
                      args.iters, dsa.HipConfig((256, 32, 8), (4096, 2048, 1024), 256, 1024))
+    elif args.workload == "prefill_hip_128k_h4":
+        _prefill_hip(synth.prefill_case("prefill_hip_S131072_h4", S=131072, H_q=4, H_kv=1, D=128, seed=4),
+                     args.iters, dsa.HipConfig((256, 32, 8), (32768, 8192, 2048), 256, 1024))
     elif args.workload == "prefill_bs_32k":
         _prefill_bs(synth.prefill_case("prefill_bs_S32768", S=32768, H_q=32, H_kv=8, D=128, seed=4),
                     args.iters)

@@ -212,6 +212,78 @@ def test_vs_and_random_lists_every_block(D):
         _check_attention(c, li, out, lse, [(0, h, m) for h in range(c.H_q) for m in range(nq)])
 
 
+def _pair_lists(rng, S, H_q, max_col):
+    """Column lists that the two query blocks of a CTA (2p, 2p + 1) share in every way:
+    identical lists, one list inside the other, partial overlap, disjoint lists, one empty
+    list; each block also lists its own diagonal block and one earlier block (columns
+    avoid both blocks' listed blocks)."""
+    nq = math.ceil(S / 64)
+    blk_cnt = np.zeros((1, H_q, nq), np.int32)
+    col_cnt = np.zeros((1, H_q, nq), np.int32)
+    blk_idx = np.full((1, H_q, nq, 2), -1, np.int32)
+    col_idx = np.full((1, H_q, nq, max_col), -1, np.int32)
+    for h in range(H_q):
+        for p in range((nq + 1) // 2):
+            ms = [m for m in (2 * p, 2 * p + 1) if m < nq]
+            bls = {}
+            for m in ms:
+                bl = sorted({m, int(rng.integers(0, m + 1))})
+                bls[m] = bl
+                blk_cnt[0, h, m] = len(bl)
+                blk_idx[0, h, m, :len(bl)] = bl
+            hi = min(S, 64 * ms[-1] + 64)
+            taken = set()
+            for m in ms:
+                taken |= set(range(64 * bls[m][0], 64 * bls[m][0] + 64)) | set(range(64 * m, 64 * m + 64))
+            pool = np.array(sorted(set(range(hi)) - taken), np.int64)
+            kind = int(rng.integers(0, 5))
+            n = min(len(pool), max_col)
+            a = rng.choice(pool, size=int(rng.integers(0, n + 1)), replace=False) if n else pool[:0]
+            if kind == 0:
+                b = a
+            elif kind == 1:
+                b = a[:len(a) // 2]
+            elif kind == 2:
+                rest = np.setdiff1d(pool, a)
+                extra = rng.choice(rest, size=min(len(rest), int(rng.integers(0, max_col - len(a) // 2 + 1))),
+                                   replace=False) if len(rest) else rest
+                b = np.concatenate([a[: len(a) // 2], extra])[:max_col]
+            elif kind == 3:
+                rest = np.setdiff1d(pool, a)
+                b = rng.choice(rest, size=min(len(rest), max_col), replace=False) if len(rest) else rest
+            else:
+                b = pool[:0]
+            for m, lst in zip(ms, (a, b)):
+                lst = np.sort(np.asarray(lst, np.int64))
+                col_cnt[0, h, m] = len(lst)
+                col_idx[0, h, m, :len(lst)] = lst
+    return blk_cnt, blk_idx, col_cnt, col_idx
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_column_lists_shared_by_block_pairs(D):
+    """Every (head, query block) against the fp64 oracle over column lists that the two
+    query blocks of a CTA share in part, in full or not at all, and over the same lists
+    in shuffled order (the kernel needs no order within a list)."""
+    rng = np.random.default_rng(90 + D)
+    c = prefill_case("pairs", S=1700, H_q=4, H_kv=2, D=D, seed=91 + D)
+    q, k, v = _dev(c)
+    blk_cnt, blk_idx, col_cnt, col_idx = _pair_lists(rng, c.S, c.H_q, max_col=420)
+    shuffled = col_idx.copy()
+    for h in range(c.H_q):
+        for m in range(shuffled.shape[2]):
+            n = int(col_cnt[0, h, m])
+            shuffled[0, h, m, :n] = rng.permutation(shuffled[0, h, m, :n])
+    t = lambda a: torch.from_numpy(a).cuda()
+    nq = math.ceil(c.S / 64)
+    for cols in (col_idx, shuffled):
+        lists = (t(blk_cnt), t(blk_idx), t(col_cnt), t(cols))
+        out, lse = dsa.sparse_attn_prefill(q, k, v, *lists)
+        torch.cuda.synchronize()
+        li = dict(zip(["blk_cnt", "blk_idx", "col_cnt", "col_idx"], lists))
+        _check_attention(c, li, out, lse, [(0, h, m) for h in range(c.H_q) for m in range(nq)])
+
+
 def test_non_positive_scale_is_rejected():
     """The kernel orders scores by their raw value; a scale <= 0 is an argument error."""
     c = prefill_case("scale", S=128, H_q=2, H_kv=1, D=64, seed=9)
