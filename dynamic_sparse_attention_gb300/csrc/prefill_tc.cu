@@ -6,16 +6,19 @@
 // "Block-Sparse FlashAttention Kernel (Appendix C.4.1)"; section 3.4 Eq. 1 with the
 // mask constant taken as exact exclusion.
 //
-// One CTA computes 128 query rows: the two consecutive 64-row query blocks m0 = 2p and
-// m1 = 2p + 1 of one head.  Keys go through the tensor core in 128-key tiles, each made
-// of two 64-key list blocks: at M = N = K = 128 the MMA runs at its full rate, while
-// 64-key tiles (Q K^T with N = 64, P V with K = 64) reach well under half of it.  The
-// CTA walks the blocks that either query block lists (the union of the two lists),
-// in descending order, and puts each next two of them into a tile (descending, so the
-// running max settles early; any two blocks, so scattered lists fill their tiles),
-// then block m0's gathered column tiles (128 columns each), then block m1's.  A row
-// masks the 64-key halves its own query block does not list, keys after it (causal)
-// and keys past the sequence end.
+// One CTA computes 128 query rows in two 64-row groups: the consecutive query blocks
+// m0 = 2p and m1 = 2p + 1 of one head, or, where two query heads of one KV head list
+// the same blocks and columns for both blocks of the pair, one query block of both
+// heads (the two CTAs of such a head pair split the pair's blocks between them).  Keys
+// go through the tensor core in 128-key tiles, each made of two 64-key list blocks: at
+// M = N = K = 128 the MMA runs at its full rate, while 64-key tiles (Q K^T with N = 64,
+// P V with K = 64) reach well under half of it.  The CTA walks the blocks that either
+// group lists (the union of the two lists), in descending order, and puts each next two
+// of them into a tile (descending, so the running max settles early; any two blocks, so
+// scattered lists fill their tiles), then group 0's gathered column tiles (128 columns
+// each), then group 1's (none when both groups share the columns: one walk serves
+// both).  A row masks the 64-key halves its own group does not list, keys after it
+// (causal) and keys past the sequence end.
 // Warp roles (352 threads):
 //   warp 0     K producer: Q once (TMA), then K tiles (two 64-row TMA boxes per 64-wide
 //              head-dim half for block tiles, 16-byte cp.async gathers for column tiles,
@@ -224,11 +227,13 @@ struct TileWalk {
   }
 };
 
-template <int D>
-__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcArgs a) {
+// The CTA's work once its row groups are chosen (HP: two query heads of one query block,
+// else two query blocks of one query head): list bitmaps, then the warp roles.  Both
+// forms are compiled separately so that each keeps the code of a fixed row layout.
+template <int D, bool HP>
+__device__ __forceinline__ void tc_cta(const TcArgs &a, unsigned char *sm, int p, int g, int b, int hl,
+                                       int hA) {
   using L = Layout<D>;
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
   uint64_t *k_full = bars, *k_empty = k_full + kKS;
   uint64_t *v_full = k_empty + kKS, *v_empty = v_full + kVS;
@@ -242,56 +247,30 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   uint32_t *bm1 = bm0 + a.n_words;
   TileMeta *meta = reinterpret_cast<TileMeta *>(sm + L::oMeta);
   const WaitCtx wc{abort_flag, a.epoch};
-
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // longest rows first; the G query heads of one KV head side by side, so the CTAs that
-  // read the same key and value rows (for lists shared by the heads, the same rows)
-  // run together and share them through L2
-  const int n_pairs = (a.n_qblk + 1) / 2;
   const int G = a.H_q / a.H_kv;
-  const int p = n_pairs - 1 - static_cast<int>(blockIdx.x) / G;
-  const int g = blockIdx.y, b = blockIdx.z;
-  const int h = g * G + static_cast<int>(blockIdx.x) % G;
-  const int m0 = 2 * p, m1 = 2 * p + 1;
+  // the two row groups: query head and query block of each, and their list rows
+  const int hq0 = HP ? hA : g * G + hl, hq1 = HP ? hA + 1 : hq0;
+  const int m0 = HP ? 2 * p + (hl & 1) : 2 * p, m1 = HP ? m0 : 2 * p + 1;
   const bool has1 = m1 < a.n_qblk;
-  const size_t bh = static_cast<size_t>(b) * a.H_q + h;
-
-  if (tid == 0) {
-    for (int i = 0; i < 2 * kKS + 2 * kVS; ++i) mbar_init(&bars[i], 1);
-    for (int i = 0; i < kSB; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], kSmWarps);   // one arrival per softmax warp
-      mbar_init(&pv_done[i], 1);
-    }
-    mbar_init(q_full, 1);
-    mbar_init(fin, 1);
-    for (int i = 0; i < 4 * 3; ++i) mbar_init(&xbar[i], kSlices);   // one arrival per key slice
-    *abort_flag = 0;
-    *n_blk_tiles_s = 0;
-    fence_mbar_init();
-  }
-  if (warp == 2) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
-  }
-  for (int w = tid; w < 2 * a.n_words; w += kThreads) bm0[w] = 0u;
-  __syncthreads();
+  const size_t lr0 = (static_cast<size_t>(b) * a.H_q + hq0) * a.n_qblk + m0;
+  const size_t lr1 = (static_cast<size_t>(b) * a.H_q + hq1) * a.n_qblk + m1;
   // tile lists -> bitmaps; a block after a half's own query block is fully masked there
   {
-    const int c_raw = a.blk_cnt[bh * a.n_qblk + m0];
+    const int c_raw = a.blk_cnt[lr0];
     DSA_CHECK(c_raw >= 0 && c_raw <= a.max_blk);
     const int c = min(max(c_raw, 0), a.max_blk);
-    const int32_t *l0 = a.blk_idx + (bh * a.n_qblk + m0) * static_cast<size_t>(a.max_blk);
+    const int32_t *l0 = a.blk_idx + lr0 * static_cast<size_t>(a.max_blk);
     for (int i = tid; i < c; i += kThreads) {
       const int n = l0[i];
       DSA_CHECK(n >= 0 && n < a.n_qblk);
       if (n >= 0 && n <= m0) atomicOr(&bm0[n >> 5], 1u << (n & 31));
     }
     if (has1) {
-      const int c1_raw = a.blk_cnt[bh * a.n_qblk + m1];
+      const int c1_raw = a.blk_cnt[lr1];
       DSA_CHECK(c1_raw >= 0 && c1_raw <= a.max_blk);
       const int c1 = min(max(c1_raw, 0), a.max_blk);
-      const int32_t *l1 = a.blk_idx + (bh * a.n_qblk + m1) * static_cast<size_t>(a.max_blk);
+      const int32_t *l1 = a.blk_idx + lr1 * static_cast<size_t>(a.max_blk);
       for (int i = tid; i < c1; i += kThreads) {
         const int n = l1[i];
         DSA_CHECK(n >= 0 && n < a.n_qblk);
@@ -311,12 +290,13 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const int n_blk_t = (*n_blk_tiles_s + 1) / 2;   // listed blocks, two per tile
-  const int cc0_raw = a.col_cnt[bh * a.n_qblk + m0];
-  const int cc1_raw = has1 ? a.col_cnt[bh * a.n_qblk + m1] : 0;
+  const int cc0_raw = a.col_cnt[lr0];
+  const int cc1_raw = has1 ? a.col_cnt[lr1] : 0;
   DSA_CHECK(cc0_raw >= 0 && cc0_raw <= a.max_col && cc1_raw >= 0 && cc1_raw <= a.max_col);
   const int c0 = min(max(cc0_raw, 0), a.max_col);
   const int c1 = has1 ? min(max(cc1_raw, 0), a.max_col) : 0;
-  const int nct0 = (c0 + kKeys - 1) / kKeys, nct1 = (c1 + kKeys - 1) / kKeys;
+  // one column walk for both groups when they list the same columns (head pairs)
+  const int nct0 = (c0 + kKeys - 1) / kKeys, nct1 = HP ? 0 : (c1 + kKeys - 1) / kKeys;
   const int T = n_blk_t + nct0 + nct1;
   const uint32_t tmem = *tmem_slot;
 
@@ -331,9 +311,12 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const uint16_t *src = (is_k ? a.k : a.v) + (static_cast<size_t>(b) * a.S * a.H_kv + g) * D;
     const size_t krow = static_cast<size_t>(a.H_kv) * D;
     if (is_k && lane == 0) {
+      // Q rows 0-63 from (hq0, block m0), 64-127 from (hq1, block m1), per head-dim half
       mbar_arrive_expect_tx(q_full, L::kHalves * L::kQHalf);
-      for (int hh = 0; hh < L::kHalves; ++hh)
-        tma_load_4d(sm + L::oQ + hh * L::kQHalf, &a.tq, q_full, 64 * hh, h, kRowsQ * p, b);
+      for (int hh = 0; hh < L::kHalves; ++hh) {
+        tma_load_4d(sm + L::oQ + hh * L::kQHalf, &a.tq, q_full, 64 * hh, hq0, kBlk * m0, b);
+        tma_load_4d(sm + L::oQ + hh * L::kQHalf + L::kQHalf / 2, &a.tq, q_full, 64 * hh, hq1, kBlk * m1, b);
+      }
     }
     TileWalk walk;
     walk.init(bm0, bm1, a.n_words);
@@ -370,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
         const int cb = (grp == 0 ? ct : ct - nct0) * kKeys;
         const int mg = grp == 0 ? m0 : m1;
         const int ncol = min(kKeys, (grp == 0 ? c0 : c1) - cb);
-        const int32_t *cl = a.col_idx + (bh * a.n_qblk + mg) * static_cast<size_t>(a.max_col);
+        const int32_t *cl = a.col_idx + (grp == 0 ? lr0 : lr1) * static_cast<size_t>(a.max_col);
         const int last_row = min(kBlk * mg + kBlk - 1, a.S - 1);
         int pos[kKeys / 32];
 #pragma unroll
@@ -394,7 +377,7 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
           below = __all_sync(kFull, below);
           if (lane == 0) {
             md->kind = 1;
-            md->mask = grp == 0 ? 0x3 : 0xC;
+            md->mask = HP ? 0xF : (grp == 0 ? 0x3 : 0xC);
             md->blk[0] = md->blk[1] = -1;
             md->below = below ? 1 : 0;
           }
@@ -494,7 +477,8 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
     const int cs = sw >> 2;            // key slice of each tile
     const int row = quarter * 32 + lane;
     const int grp = row >> 6;
-    const int qpos = kRowsQ * p + row;
+    const int qpos = kBlk * (grp == 0 ? m0 : m1) + (row & (kBlk - 1));
+    const int hrow = grp == 0 ? hq0 : hq1;   // the row's query head
     const bool row_ok = qpos < a.S;
     const uint32_t tl = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     constexpr int kOS = D / kSlices;   // O columns this warp rescales and stores
@@ -714,21 +698,100 @@ __global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_co
 #pragma unroll
       for (int i = 0; i < kOS / 2; ++i)
         w[i] = good ? pack_bf16x2(__uint_as_float(o[2 * i]) * inv, __uint_as_float(o[2 * i + 1]) * inv) : 0u;
-      uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((static_cast<size_t>(b) * a.S + qpos) * a.H_q + h) * D +
+      uint4 *dst = reinterpret_cast<uint4 *>(a.out + ((static_cast<size_t>(b) * a.S + qpos) * a.H_q + hrow) * D +
                                              cs * kOS);
 #pragma unroll
       for (int i = 0; i < kOS / 8; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
-      if (cs == 0 && a.lse) a.lse[bh * a.S + qpos] = good ? (m_cur + log2f(lt)) * kLn2 : -INFINITY;
+      if (cs == 0 && a.lse)
+        a.lse[(static_cast<size_t>(b) * a.H_q + hrow) * a.S + qpos] = good ? (m_cur + log2f(lt)) * kLn2 : -INFINITY;
     }
   }
 
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, 1) prefill_tc_kernel(const __grid_constant__ TcArgs a) {
+  using L = Layout<D>;
+  extern __shared__ unsigned char smem_raw[];
+  unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t *bars = reinterpret_cast<uint64_t *>(sm + L::oBar);
+  uint64_t *k_full = bars, *k_empty = k_full + kKS;
+  uint64_t *v_full = k_empty + kKS, *v_empty = v_full + kVS;
+  uint64_t *s_full = v_empty + kVS, *p_full = s_full + kSB;
+  uint64_t *pv_done = p_full + kSB, *q_full = pv_done + kSB, *fin = q_full + 1;
+  uint64_t *xbar = fin + 1;   // [4 quarters][3]: row-max exchange by tile parity, row sums
+  uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + L::oMisc);
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + L::oMisc + 4);
+  int *n_blk_tiles_s = reinterpret_cast<int *>(sm + L::oMisc + 8);
+  uint32_t *bm0 = reinterpret_cast<uint32_t *>(sm + L::oBits);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // longest rows first; the G query heads of one KV head side by side, so the CTAs that
+  // read the same key and value rows (for lists shared by the heads, the same rows)
+  // run together and share them through L2
+  const int n_pairs = (a.n_qblk + 1) / 2;
+  const int G = a.H_q / a.H_kv;
+  const int hl = static_cast<int>(blockIdx.x) % G;   // query head within the KV head
+  const int p = n_pairs - 1 - static_cast<int>(blockIdx.x) / G;
+  const int g = blockIdx.y, b = blockIdx.z;
+  // The CTA's 128 rows are two 64-row groups, each one (query head, query block).  The
+  // two CTAs of query heads hA = 2i, hA + 1 of a KV head at pair p share the four rows
+  // (hA, hA + 1) x (2p, 2p + 1): when both heads list the same blocks and columns for
+  // both query blocks (lists made once for every head, as the InfiniteHiP ones are), CTA
+  // hl & 1 takes query block 2p + (hl & 1) of both heads, so that every tile serves all
+  // 128 rows; otherwise each takes its own head's blocks 2p and 2p + 1.
+  const int hA = g * G + (hl & ~1);
+  const bool quad = (hl | 1) < G && 2 * p + 1 < a.n_qblk;
+  bool differ = !quad;
+  if (quad) {
+    const size_t rA = (static_cast<size_t>(b) * a.H_q + hA) * a.n_qblk, rB = rA + a.n_qblk;
+#pragma unroll 1
+    for (int m = 2 * p; m <= 2 * p + 1 && !differ; ++m) {
+      const int nb = min(max(a.blk_cnt[rA + m], 0), a.max_blk), nc = min(max(a.col_cnt[rA + m], 0), a.max_col);
+      if (nb != min(max(a.blk_cnt[rB + m], 0), a.max_blk) || nc != min(max(a.col_cnt[rB + m], 0), a.max_col)) {
+        differ = true;
+        break;
+      }
+      const int32_t *ba = a.blk_idx + (rA + m) * static_cast<size_t>(a.max_blk);
+      const int32_t *bb = a.blk_idx + (rB + m) * static_cast<size_t>(a.max_blk);
+      for (int i = tid; i < nb; i += kThreads) differ |= ba[i] != bb[i];
+      if (nc > 0) {
+        const int32_t *ca = a.col_idx + (rA + m) * static_cast<size_t>(a.max_col);
+        const int32_t *cb = a.col_idx + (rB + m) * static_cast<size_t>(a.max_col);
+        for (int i = tid; i < nc; i += kThreads) differ |= ca[i] != cb[i];
+      }
+    }
+  }
+
+  if (tid == 0) {
+    for (int i = 0; i < 2 * kKS + 2 * kVS; ++i) mbar_init(&bars[i], 1);
+    for (int i = 0; i < kSB; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&p_full[i], kSmWarps);   // one arrival per softmax warp
+      mbar_init(&pv_done[i], 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(fin, 1);
+    for (int i = 0; i < 4 * 3; ++i) mbar_init(&xbar[i], kSlices);   // one arrival per key slice
+    *abort_flag = 0;
+    *n_blk_tiles_s = 0;
+    fence_mbar_init();
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  for (int w = tid; w < 2 * a.n_words; w += kThreads) bm0[w] = 0u;
+  const bool head_pair = __syncthreads_or(differ ? 1 : 0) == 0;
+  if (head_pair) tc_cta<D, true>(a, sm, p, g, b, hl, hA);
+  else tc_cta<D, false>(a, sm, p, g, b, hl, hA);
   tc_fence_before();
   __syncthreads();
   if (warp == 2) {
     tc_fence_after();
     if (lane == 0) drain_wait(fin, 0, 1000000000ull);   // every MMA retired before TMEM is freed
     __syncwarp();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(*tmem_slot, kTmemCols);
   }
   if (tid == 0 && *abort_flag) atomicExch(&g_prefill_tc_error, 1);
 }
@@ -772,7 +835,7 @@ template <int D>
 cudaError_t launch_tc_d(const PrefillArgs &pa, cudaStream_t s) {
   TcArgs a;
   std::memset(&a, 0, sizeof(a));
-  if (!make_bshd_map(&a.tq, pa.q, D, pa.H_q, pa.S, pa.B, kRowsQ) ||
+  if (!make_bshd_map(&a.tq, pa.q, D, pa.H_q, pa.S, pa.B, kBlk) ||
       !make_bshd_map(&a.tk, pa.k, D, pa.H_kv, pa.S, pa.B, kBlk) ||
       !make_bshd_map(&a.tv, pa.v, D, pa.H_kv, pa.S, pa.B, kBlk))
     return cudaErrorInvalidValue;

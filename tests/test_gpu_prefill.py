@@ -284,6 +284,34 @@ def test_column_lists_shared_by_block_pairs(D):
         _check_attention(c, li, out, lse, [(0, h, m) for h in range(c.H_q) for m in range(nq)])
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_lists_shared_by_head_pairs(D):
+    """Every (head, query block) against the fp64 oracle when the two query heads of a
+    head pair list the same blocks and columns for some query-block pairs (both blocks),
+    for one block of a pair only, or not at all: the kernel takes the head-pair row
+    groups exactly where both blocks' lists agree; G = 4, an odd query-block count."""
+    rng = np.random.default_rng(110 + D)
+    c = prefill_case("heads", S=1600, H_q=8, H_kv=2, D=D, seed=111 + D)
+    q, k, v = _dev(c)
+    lists = [x.cpu().numpy() for x in _random_lists(rng, c.S, c.H_q, max_blk=20, max_col=300)]
+    blk_cnt, blk_idx, col_cnt, col_idx = lists
+    nq = math.ceil(c.S / 64)
+    for h0 in range(0, c.H_q, 2):
+        for p in range((nq + 1) // 2):
+            kind = (h0 // 2 + p) % 3   # 0: both blocks shared, 1: block 2p only, 2: none
+            ms = [2 * p, 2 * p + 1] if kind == 0 else ([2 * p] if kind == 1 else [])
+            for m in ms:
+                if m < nq:
+                    for a in lists:
+                        a[0, h0 + 1, m] = a[0, h0, m]
+    t = lambda a: torch.from_numpy(a).cuda()
+    tl = tuple(t(a) for a in lists)
+    out, lse = dsa.sparse_attn_prefill(q, k, v, *tl)
+    torch.cuda.synchronize()
+    li = dict(zip(["blk_cnt", "blk_idx", "col_cnt", "col_idx"], tl))
+    _check_attention(c, li, out, lse, [(0, h, m) for h in range(c.H_q) for m in range(nq)])
+
+
 def test_non_positive_scale_is_rejected():
     """The kernel orders scores by their raw value; a scale <= 0 is an argument error."""
     c = prefill_case("scale", S=128, H_q=2, H_kv=1, D=64, seed=9)
