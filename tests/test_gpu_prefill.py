@@ -312,6 +312,55 @@ def test_lists_shared_by_head_pairs(D):
     _check_attention(c, li, out, lse, [(0, h, m) for h in range(c.H_q) for m in range(nq)])
 
 
+def _run_lists(rng, S, H_q, max_col):
+    """Column lists made of runs of consecutive keys (lengths 8, 5, 16, 1 in a random
+    mix), ascending, outside the block's two listed blocks."""
+    nq = math.ceil(S / 64)
+    blk_cnt = np.zeros((1, H_q, nq), np.int32)
+    col_cnt = np.zeros((1, H_q, nq), np.int32)
+    blk_idx = np.full((1, H_q, nq, 2), -1, np.int32)
+    col_idx = np.full((1, H_q, nq, max_col), -1, np.int32)
+    for h in range(H_q):
+        for m in range(nq):
+            bl = sorted({m, int(rng.integers(0, m + 1))})
+            blk_cnt[0, h, m] = len(bl)
+            blk_idx[0, h, m, :len(bl)] = bl
+            free = np.ones(min(S, 64 * m + 64), bool)
+            for n in bl:
+                free[64 * n:64 * n + 64] = False
+            keys = []
+            x = int(rng.integers(0, 20))
+            while x < len(free) and len(keys) < max_col:
+                run = int(rng.choice([8, 8, 8, 5, 16, 1]))
+                seg = [y for y in range(x, min(x + run, len(free))) if free[y]]
+                keys += seg[:max_col - len(keys)]
+                x += run + int(rng.integers(0, 40))
+            col_cnt[0, h, m] = len(keys)
+            col_idx[0, h, m, :len(keys)] = keys
+    return blk_cnt, blk_idx, col_cnt, col_idx
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_column_runs(D):
+    """Every (head, query block) against the fp64 oracle over column lists made of runs
+    of consecutive keys, as the InfiniteHiP selection of consecutive-token chunks makes
+    them, the same lists for the two heads of one head pair (head-pair row groups) and
+    different ones for the other pair."""
+    rng = np.random.default_rng(130 + D)
+    c = prefill_case("runs", S=2100, H_q=4, H_kv=2, D=D, seed=131 + D)
+    q, k, v = _dev(c)
+    lists = _run_lists(rng, c.S, c.H_q, max_col=500)
+    for a in lists:
+        a[0, 1] = a[0, 0]   # heads 0 and 1 (one head pair of KV head 0) share their lists
+    t = lambda a: torch.from_numpy(a).cuda()
+    tl = tuple(t(a) for a in lists)
+    out, lse = dsa.sparse_attn_prefill(q, k, v, *tl)
+    torch.cuda.synchronize()
+    li = dict(zip(["blk_cnt", "blk_idx", "col_cnt", "col_idx"], tl))
+    nq = math.ceil(c.S / 64)
+    _check_attention(c, li, out, lse, [(0, h, m) for h in range(c.H_q) for m in range(nq)])
+
+
 def test_non_positive_scale_is_rejected():
     """The kernel orders scores by their raw value; a scale <= 0 is an argument error."""
     c = prefill_case("scale", S=128, H_q=2, H_kv=1, D=64, seed=9)
