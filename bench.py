@@ -47,7 +47,7 @@ NOMINAL_BF16_TFLOPS = 2250.0
 CACHE_PRESETS = {"default": (16, 8, 4, 4), "flash": (96, 24, 8, 8)}
 NCU_TRAFFIC = {
     ("hip_stage_score_s0", "decode_gqa_T1048576"): 201637120 + 3022080,
-    ("prefill_attention_tc", "prefill_vs_S131072"): 4342123392 + 1072366208,
+    ("prefill_attention_tc", "prefill_vs_S131072"): 3470680960 + 1056529664,
 }
 
 
