@@ -158,21 +158,43 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
     }
   }
   if (!QREG) {
-    const int n = a.T_q * a.H_q * D;
-    for (int e = threadIdx.x; e < n; e += blockDim.x) {
-      if constexpr (sizeof(TQ) == 2) s_q[e] = bf16_to_f32(reinterpret_cast<const uint16_t *>(q)[e]);
-      else s_q[e] = reinterpret_cast<const float *>(q)[e];
+    // the query rows as fp32, 16-byte loads, independent across the unrolled iterations
+    // (a one-warp CTA loads T_q * H_q * D elements)
+    const int n8 = a.T_q * a.H_q * D / 8;   // D is a multiple of 8
+#pragma unroll 8
+    for (int e = threadIdx.x; e < n8; e += blockDim.x) {
+      float4 lo, hi;
+      if constexpr (sizeof(TQ) == 2) {
+        const uint4 w = __ldg(reinterpret_cast<const uint4 *>(q) + e);
+        lo = make_float4(bf16_lo(w.x), bf16_hi(w.x), bf16_lo(w.y), bf16_hi(w.y));
+        hi = make_float4(bf16_lo(w.z), bf16_hi(w.z), bf16_lo(w.w), bf16_hi(w.w));
+      } else {
+        lo = __ldg(reinterpret_cast<const float4 *>(q) + 2 * e);
+        hi = __ldg(reinterpret_cast<const float4 *>(q) + 2 * e + 1);
+      }
+      reinterpret_cast<float4 *>(s_q)[2 * e] = lo;
+      reinterpret_cast<float4 *>(s_q)[2 * e + 1] = hi;
     }
   }
   if (ROWS) cp_async_wait<0>();
   __syncthreads();
 
-  const int h = threadIdx.x >> 3, sub = threadIdx.x & 7;
+  // Octet o (eight lanes) scores for head o % H_q.  With several query rows and fewer
+  // than four heads, the warp's spare octets take a share of the rows (octet o the rows
+  // t = o / H_q (mod RS)) and the RS octets of a head combine their row maxima, so the
+  // tournament of every head runs on all of them alike.
+  const int oct = threadIdx.x >> 3, sub = threadIdx.x & 7;
+  const int RS = QREG ? 1 : max(1, static_cast<int>(blockDim.x >> 3) / a.H_q);   // 4, 2 or 1 when T_q > 1
+  const int h = QREG ? oct : oct % a.H_q, rs = QREG ? 0 : oct / a.H_q;
   const int G = a.H_q / a.H_kv;
   const int n_here = min(C, n_chunk - j0);   // chunks of this CTA that exist
-  if (h < a.H_q) {
+  if (QREG ? h < a.H_q : rs < RS) {
     const int g = h / G;
     const unsigned omask = 0xffu << (threadIdx.x & 24);
+    // the lanes of all RS octets of this head (RS > 1 only in one-warp CTAs)
+    unsigned hmask = 0u;
+    for (int r = 0; r < RS; ++r) hmask |= 0xffu << (8 * (h + r * a.H_q));
+    if (RS == 1) hmask = omask;
     constexpr int NV = EPL * static_cast<int>(sizeof(TK)) / 16;    // 16-byte key loads per lane
     constexpr int NVQ = EPL * static_cast<int>(sizeof(TQ)) / 16;   // and query loads
     static_assert(NV >= 1, "a lane's key slice is at least 16 bytes");
@@ -207,7 +229,7 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
           for (int i = 0; i < NV; ++i) raw[i] = __ldg(kp + i);
         }
         float best = -INFINITY;
-        for (int t = 0; t < T_q; ++t) {
+        for (int t = rs; t < T_q; t += RS) {
           const float *qq = s_q + (static_cast<size_t>(t) * a.H_q + h) * D + sub * EPL;
           float d = 0.f;
           if constexpr (std::is_same<TQ, TK>::value && sizeof(TK) == 2 && QREG) {
@@ -267,6 +289,8 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
           d += __shfl_xor_sync(omask, d, 1);
           best = fmaxf(best, d);
         }
+        // the head's other octets hold the maxima of its other rows
+        for (int o = 8 * a.H_q; o < 8 * a.H_q * RS; o <<= 1) best = fmaxf(best, __shfl_xor_sync(hmask, best, o));
         return best;
       };
       // The first kWarmLevels probes of every head's tournament can only be one of the
@@ -297,7 +321,7 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
         }
       };
       if constexpr (kWarmLevels > 0 && !ROWS) {
-        if ((sub & 3) == 0) warm();   // two lanes per row: one per 128-byte line
+        if ((sub & 3) == 0 && rs == 0) warm();   // two lanes per row: one per 128-byte line
       }
       // SelectRep: halve [lo, hi] at the rounded-up midpoint; the right half wins only
       // when its first token scores strictly higher than the left half's first token.
@@ -313,7 +337,7 @@ __global__ void __launch_bounds__(NT_MAX, MIN_B) stage_score_kernel(StageScoreAr
           hi = mid - 1;
         }
       }
-      if (sub == 0) {
+      if (sub == 0 && rs == 0) {
         s_rho[c * a.H_q + h] = s_lo;
         if (a.dbg_rep) {
           const size_t o = (static_cast<size_t>(b) * a.H_q + h) * a.max_chunks + j;
